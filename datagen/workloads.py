@@ -1,0 +1,112 @@
+"""Named synthetic attention workloads (shapes, seeds, value distributions).
+
+Each workload is described by what it is and its sizes.  Inputs are drawn with
+:mod:`datagen` and returned as CPU tensors; callers move them to the device.
+
+Recipe (shared by tests, the benchmark and the oracle's timing sample):
+  * Q, K, V entries are i.i.d. N(0, 1) float32 draws rounded to bf16 (or fp16),
+    streams 0, 1, 2 of the workload's seed;
+  * the fp8 workload replaces each entry independently with probability 1e-3 by
+    an N(0, 10^2) draw (streams +1000 / +2000 of the same stream), and draws a
+    random sign vector of length d for the Hadamard rotation;
+  * the varlen workload draws 32 integer lengths uniform on [64, 4096]
+    (stream 10) and packs the sequences back to back.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+
+from . import normal, outlier_normal, random_signs, to_bf16, to_fp16, uniform_int
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str            # "bf16", "fp16" or "fp8" (fp8: bf16 inputs quantised on device)
+    B: int
+    H: int
+    N: int                # sequence length (dense); max length (varlen)
+    d: int
+    causal: bool
+    seed: int
+    lengths: Optional[List[int]] = None   # varlen only
+    outliers: bool = False
+
+    @property
+    def varlen(self) -> bool:
+        return self.lengths is not None
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+    @property
+    def tokens(self) -> int:
+        return int(sum(self.lengths)) if self.varlen else self.B * self.N
+
+    def flops(self) -> float:
+        """Attention-forward FLOP count 4*B*H*N^2*d, halved when causal; for
+        varlen the per-sequence counts are summed."""
+        if self.varlen:
+            f = sum(4.0 * self.H * L * L * self.d for L in self.lengths)
+        else:
+            f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2.0 if self.causal else f
+
+    def cu_seqlens(self) -> np.ndarray:
+        if self.varlen:
+            lens = np.asarray(self.lengths, dtype=np.int64)
+        else:
+            lens = np.full(self.B, self.N, dtype=np.int64)
+        return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+
+def _shape(w: Workload):
+    return (w.tokens, w.H, w.d) if w.varlen else (w.B, w.N, w.H, w.d)
+
+
+def make_inputs(w: Workload) -> dict:
+    """Seeded Q, K, V (CPU tensors, bf16 or fp16; layout [B,N,H,d] dense or
+    [T,H,d] packed), plus cu_seqlens (int32) and, for fp8, the sign vector."""
+    shape = _shape(w)
+    conv = to_fp16 if w.dtype == "fp16" else to_bf16
+    out = {}
+    for s, nm in enumerate("qkv"):
+        if w.outliers:
+            x = outlier_normal(w.seed, s, shape)
+        else:
+            x = normal(w.seed, s, shape)
+        out[nm] = conv(x)
+    out["cu_seqlens"] = w.cu_seqlens()
+    if w.dtype == "fp8":
+        out["signs"] = random_signs(w.seed, w.d)
+    return out
+
+
+def varlen_lengths(seed: int, nseq: int, lo: int, hi: int) -> List[int]:
+    return [int(x) for x in uniform_int(seed, 10, nseq, lo, hi)]
+
+
+# The five workloads the method is measured on.
+TINY = Workload("bf16 non-causal B=1 H=1 N=128 d=64", "bf16", 1, 1, 128, 64, False, 1001)
+DENSE = Workload("bf16 non-causal B=4 H=16 N=8448 d=128", "bf16", 4, 16, 8448, 128, False, 1002)
+FP8 = Workload("fp8 e4m3 non-causal B=4 H=16 N=8192 d=128, 0.1% outliers",
+               "fp8", 4, 16, 8192, 128, False, 1003, outliers=True)
+
+
+def causal_sweep() -> List[Workload]:
+    out = []
+    for (H, d) in ((16, 128), (32, 64)):
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            out.append(Workload(f"bf16 causal B={16384 // N} H={H} N={N} d={d}",
+                                "bf16", 16384 // N, H, N, d, True, 1004))
+    return out
+
+
+def varlen_causal() -> Workload:
+    lens = varlen_lengths(1005, 32, 64, 4096)
+    return Workload("bf16 causal varlen 32 seqs L~U[64,4096] H=32 d=128", "bf16",
+                    32, 32, max(lens), 128, True, 1005, lengths=lens)

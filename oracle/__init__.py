@@ -1,0 +1,235 @@
+"""fp64 CPU oracle for the fused attention forward pass -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+binding) never loads it and shares no code with it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64).  This module only
+compiles it with gcc, loads it with ctypes and marshals numpy arrays.
+
+What each function restates:
+  * :func:`attention`, :func:`attention_rows`, :func:`probs` -- exact attention,
+    "Fused attention kernel" (wikillm concept card), Overview and
+    Implementation sketch: O = softmax(scale * Q K^T) V per sequence (causal:
+    top-left aligned), lse = M + log Z in natural-log units;
+  * :func:`rotate`, :func:`hadamard_matrix` -- incoherent processing, same card,
+    "8-bit forward pass (FP8, Hopper)": x -> x * diag(signs) * H_d / sqrt(d);
+  * :func:`e4m3_encode`, :func:`e4m3_decode`, :func:`block_quant`,
+    :func:`quantize_qkv` -- e4m3 block quantisation, same section: one scale
+    per 128-token block of one (batch, head), scale = amax / 448.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i8p = ctypes.POINTER(ctypes.c_int8)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into oracle/_build/liboracle.so (portable C, no
+    architecture-specific flags)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+                           "-lm", "-lpthread"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.oracle_attention_rows.argtypes = [
+            _dp, _dp, _dp, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_double, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp, _dp,
+            ctypes.c_int32]
+        lib.oracle_attention_probs.argtypes = [
+            _dp, _dp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+            ctypes.c_int32, _dp]
+        lib.oracle_hadamard_matrix.argtypes = [ctypes.c_int32, _dp]
+        lib.oracle_rotate.argtypes = [_dp, ctypes.c_int64, ctypes.c_int32, _i8p, _dp]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode_array.argtypes = [_dp, ctypes.c_int64, _u8p]
+        lib.oracle_e4m3_decode_array.argtypes = [_u8p, ctypes.c_int64, _dp]
+        lib.oracle_block_quant.argtypes = [
+            _dp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_int32, _u8p, _dp]
+        _lib = lib
+        return lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact up-conversion to a contiguous float64 array (accepts numpy arrays
+    and CPU torch tensors of any float dtype, bf16/fp16 included)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def attention_rows(q, k, v, cu_seqlens, scale: float, causal: bool, row_tok, row_head,
+                   nthreads: int | None = None):
+    """O [nrows, d] and lse [nrows] for the packed layout q, k, v [T, H, d]."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, d = q.shape
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    rt = np.ascontiguousarray(row_tok, dtype=np.int64)
+    rh = np.ascontiguousarray(row_head, dtype=np.int32)
+    n = rt.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_attention_rows(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(cu, _i32p),
+                                   len(cu) - 1, H, d, float(scale), int(bool(causal)),
+                                   _ptr(rt, _i64p), _ptr(rh, _i32p), n,
+                                   _ptr(o, _dp), _ptr(lse, _dp),
+                                   nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows failed ({rc})")
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens, scale: float, causal: bool, nthreads=None):
+    """Full O [T, H, d] and lse [H, T] for packed sequences."""
+    q = _f64(q)
+    T, H, d = q.shape
+    tok = np.repeat(np.arange(T, dtype=np.int64), H)
+    head = np.tile(np.arange(H, dtype=np.int32), T)
+    o, lse = attention_rows(q, k, v, cu_seqlens, scale, causal, tok, head, nthreads)
+    return o.reshape(T, H, d), lse.reshape(T, H).T.copy()
+
+
+def attention(q, k, v, scale: float, causal: bool, nthreads=None):
+    """Full O [B, N, H, d] and lse [B, H, N] for a dense batch [B, N, H, d]."""
+    q = _f64(q)
+    B, N, H, d = q.shape
+    cu = (np.arange(B + 1) * N).astype(np.int32)
+    o, lse = attention_varlen(q.reshape(B * N, H, d), _f64(k).reshape(B * N, H, d),
+                              _f64(v).reshape(B * N, H, d), cu, scale, causal, nthreads)
+    return o.reshape(B, N, H, d), lse.reshape(H, B, N).transpose(1, 0, 2).copy()
+
+
+def probs(q, k, scale: float, causal: bool):
+    """P [H, N, N] of one sequence q, k [N, H, d] (small shapes only)."""
+    lib = _load()
+    q, k = _f64(q), _f64(k)
+    N, H, d = q.shape
+    p = np.empty((H, N, N), dtype=np.float64)
+    rc = lib.oracle_attention_probs(_ptr(q, _dp), _ptr(k, _dp), N, H, d, float(scale),
+                                    int(bool(causal)), _ptr(p, _dp))
+    if rc != 0:
+        raise ValueError("oracle_attention_probs failed")
+    return p
+
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    lib = _load()
+    hm = np.empty((d, d), dtype=np.float64)
+    if lib.oracle_hadamard_matrix(d, _ptr(hm, _dp)) != 0:
+        raise ValueError("d must be a power of two")
+    return hm
+
+
+def rotate(x, signs) -> np.ndarray:
+    """x [..., d] -> x * diag(signs) * H_d / sqrt(d) (signs None: no sign flip)."""
+    lib = _load()
+    x = _f64(x)
+    d = x.shape[-1]
+    flat = x.reshape(-1, d)
+    out = np.empty_like(flat)
+    sg = None if signs is None else np.ascontiguousarray(signs, dtype=np.int8)
+    rc = lib.oracle_rotate(_ptr(flat, _dp), flat.shape[0], d,
+                           None if sg is None else _ptr(sg, _i8p), _ptr(out, _dp))
+    if rc != 0:
+        raise ValueError("oracle_rotate failed")
+    return out.reshape(x.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    lib = _load()
+    x = _f64(x)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape[0], dtype=np.uint8)
+    lib.oracle_e4m3_encode_array(_ptr(flat, _dp), flat.shape[0], _ptr(out, _u8p))
+    return out.reshape(x.shape)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    flat = c.reshape(-1)
+    out = np.empty(flat.shape[0], dtype=np.float64)
+    lib.oracle_e4m3_decode_array(_ptr(flat, _u8p), flat.shape[0], _ptr(out, _dp))
+    return out.reshape(c.shape)
+
+
+def block_quant(x, per_tensor: bool = False, block: int = 128):
+    """codes uint8 [B,N,H,d] and descale float64 [B,H,ceil(N/block)] of x [B,N,H,d]."""
+    lib = _load()
+    x = _f64(x)
+    B, N, H, d = x.shape
+    nblk = (N + block - 1) // block
+    codes = np.empty(x.shape, dtype=np.uint8)
+    desc = np.empty((B, H, nblk), dtype=np.float64)
+    rc = lib.oracle_block_quant(_ptr(x, _dp), B, N, H, d, block, int(bool(per_tensor)),
+                                _ptr(codes, _u8p), _ptr(desc, _dp))
+    if rc != 0:
+        raise ValueError("oracle_block_quant failed")
+    return codes, desc
+
+
+def quantize_qkv(q, k, v, signs, per_tensor: bool = False, block: int = 128):
+    """The fp8 pre-step in the pages' order: rotate Q and K by
+    diag(signs) * H_d / sqrt(d) (skipped when signs is None), then quantise Q,
+    K and V to e4m3 with block (or per-tensor) scales.  Returns a dict with the
+    codes, descales and the rotated fp64 values that were quantised."""
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    if signs is not None:
+        qf, kf = rotate(qf, signs), rotate(kf, signs)
+    out = {"q_rot": qf, "k_rot": kf}
+    for nm, x in (("q", qf), ("k", kf), ("v", vf)):
+        out[nm + "8"], out["d" + nm] = block_quant(x, per_tensor, block)
+    return out
+
+
+def dequantize(codes, descale, block: int = 128) -> np.ndarray:
+    """decode(code) * descale of its block, [B,N,H,d]."""
+    x = e4m3_decode(codes)
+    B, N, H, d = x.shape
+    blk = np.arange(N) // block
+    s = np.asarray(descale, dtype=np.float64)[:, :, blk]          # [B, H, N]
+    return x * s.transpose(0, 2, 1)[..., None]

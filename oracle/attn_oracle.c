@@ -1,0 +1,344 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE, not part of the product path.
+ *
+ * A plain, slow, fp64 CPU statement of what the fused attention forward pass
+ * computes.  Only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg may load this library.  It shares no code, header, table or constant
+ * with the CUDA path.
+ *
+ * Sources (the pages this restates):
+ *  - "Fused attention kernel" (wikillm concept card), section Overview: exact
+ *    attention is softmax of the score matrix times V; the fused kernel only
+ *    reorganises that computation, so the result it must reach is the plain
+ *    definition below.
+ *  - same card, section Implementation sketch: the outputs are O and the
+ *    row log-sum-exp  lse = m + log(l)  (natural log).
+ *  - same card, section "8-bit forward pass (FP8, Hopper)": e4m3 format,
+ *    one scale per block of Q, K and V, and incoherent processing, i.e. Q and
+ *    K multiplied by an orthogonal matrix built from a random sign diagonal
+ *    and a Hadamard matrix.
+ *
+ * Readings where the pages leave a step open (each also listed in the design
+ * notes):
+ *  - scores are scale * q.k (the sketch omits the scale; the problem statement
+ *    carries it); lse is in natural-log units of the scaled scores;
+ *  - causal masking is top-left aligned: query i sees keys j <= i of its own
+ *    sequence;
+ *  - the orthogonal matrix is M = D * H_d / sqrt(d) with H_d the Sylvester
+ *    Hadamard matrix, H[i][j] = (-1)^popcount(i & j), and D = diag(signs);
+ *  - a block scale is amax(|x|)/448 (448 = largest finite e4m3 value), an
+ *    all-zero block takes scale 1, and codes are round-to-nearest-even with
+ *    saturation to +-448.
+ *
+ * Every function returns 0 on success and a negative value on bad arguments.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Exact attention for a list of query rows.                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const double *q, *k, *v;
+    const int32_t *cu;
+    int32_t nseq, H, d, causal;
+    double scale;
+    const int64_t *row_tok;
+    const int32_t *row_head;
+    int64_t r0, r1;
+    double *o, *lse;
+    int status;
+} rows_job;
+
+/* Sequence index s with cu[s] <= t < cu[s+1], or -1. */
+static int32_t seq_of(const int32_t *cu, int32_t nseq, int64_t t)
+{
+    int32_t lo = 0, hi = nseq - 1;
+    if (nseq <= 0 || t < cu[0] || t >= cu[nseq]) return -1;
+    while (lo < hi) {
+        int32_t mid = (lo + hi + 1) / 2;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+static void *rows_worker(void *arg)
+{
+    rows_job *jb = (rows_job *)arg;
+    const int32_t H = jb->H, d = jb->d;
+    const int64_t tok_stride = (int64_t)H * d;
+    int64_t maxlen = 0;
+    for (int32_t s = 0; s < jb->nseq; ++s) {
+        int64_t L = (int64_t)jb->cu[s + 1] - jb->cu[s];
+        if (L > maxlen) maxlen = L;
+    }
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!sc) { jb->status = -2; return NULL; }
+
+    for (int64_t r = jb->r0; r < jb->r1; ++r) {
+        const int64_t t = jb->row_tok[r];
+        const int32_t h = jb->row_head[r];
+        double *orow = jb->o + r * d;
+        const int32_t s = seq_of(jb->cu, jb->nseq, t);
+        if (s < 0 || h < 0 || h >= H) { jb->status = -1; break; }
+        const int64_t start = jb->cu[s];
+        const int64_t L = (int64_t)jb->cu[s + 1] - start;
+        const int64_t i = t - start;                 /* position in its sequence */
+        const int64_t nkeys = jb->causal ? i + 1 : L; /* allowed keys j < nkeys */
+
+        const double *qrow = jb->q + t * tok_stride + (int64_t)h * d;
+        /* scores s_j = scale * sum_c q_c k_jc, and their maximum */
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            const double *krow = jb->k + (start + j) * tok_stride + (int64_t)h * d;
+            double acc = 0.0;
+            for (int32_t c = 0; c < d; ++c) acc += qrow[c] * krow[c];
+            sc[j] = jb->scale * acc;
+            if (sc[j] > mx) mx = sc[j];
+        }
+        if (nkeys == 0) {            /* no allowed key: O = 0, lse = -inf */
+            for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+            jb->lse[r] = -INFINITY;
+            continue;
+        }
+        /* Z = sum_j exp(s_j - M);  O = sum_j exp(s_j - M) v_j / Z */
+        double z = 0.0;
+        for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            const double w = exp(sc[j] - mx);
+            const double *vrow = jb->v + (start + j) * tok_stride + (int64_t)h * d;
+            z += w;
+            for (int32_t c = 0; c < d; ++c) orow[c] += w * vrow[c];
+        }
+        for (int32_t c = 0; c < d; ++c) orow[c] /= z;
+        jb->lse[r] = mx + log(z);
+    }
+    free(sc);
+    return NULL;
+}
+
+/*
+ * O and LSE for the query rows (row_tok[r], row_head[r]), r < nrows.
+ * q, k, v: packed [T, H, d] (token-major); sequence s holds tokens
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1.  A dense [B, N, H, d] batch is the
+ * same bytes with cu_seqlens = 0, N, 2N, ...
+ * o: [nrows, d]; lse: [nrows].
+ */
+int oracle_attention_rows(const double *q, const double *k, const double *v,
+                          const int32_t *cu_seqlens, int32_t nseq,
+                          int32_t H, int32_t d, double scale, int32_t causal,
+                          const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
+                          double *o, double *lse, int32_t nthreads)
+{
+    if (!q || !k || !v || !cu_seqlens || !row_tok || !row_head || !o || !lse) return -1;
+    if (nseq < 1 || H < 1 || d < 1 || nrows < 0) return -1;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > nrows) nthreads = nrows > 0 ? (int32_t)nrows : 1;
+
+    rows_job jobs[256];
+    pthread_t th[256];
+    for (int32_t w = 0; w < nthreads; ++w) {
+        rows_job *jb = &jobs[w];
+        jb->q = q; jb->k = k; jb->v = v; jb->cu = cu_seqlens; jb->nseq = nseq;
+        jb->H = H; jb->d = d; jb->causal = causal; jb->scale = scale;
+        jb->row_tok = row_tok; jb->row_head = row_head;
+        jb->r0 = nrows * w / nthreads; jb->r1 = nrows * (w + 1) / nthreads;
+        jb->o = o; jb->lse = lse; jb->status = 0;
+    }
+    for (int32_t w = 1; w < nthreads; ++w)
+        if (pthread_create(&th[w], NULL, rows_worker, &jobs[w]) != 0)
+            jobs[w].status = -3;                   /* not started: run it inline below */
+    rows_worker(&jobs[0]);
+    int status = jobs[0].status;
+    for (int32_t w = 1; w < nthreads; ++w) {
+        if (jobs[w].status == -3) { jobs[w].status = 0; rows_worker(&jobs[w]); }
+        else pthread_join(th[w], NULL);
+        if (jobs[w].status < 0) status = jobs[w].status;
+    }
+    return status;
+}
+
+/*
+ * Probability matrix of one sequence, for small checks: P[h][i][j] =
+ * exp(s_ij - M_i) / Z_i over the allowed keys, 0 elsewhere.
+ * q, k: [N, H, d]; p: [H, N, N].
+ */
+int oracle_attention_probs(const double *q, const double *k, int32_t N, int32_t H, int32_t d,
+                           double scale, int32_t causal, double *p)
+{
+    if (!q || !k || !p || N < 1 || H < 1 || d < 1) return -1;
+    const int64_t ts = (int64_t)H * d;
+    for (int32_t h = 0; h < H; ++h) {
+        for (int32_t i = 0; i < N; ++i) {
+            double *prow = p + ((int64_t)h * N + i) * N;
+            const int32_t nk = causal ? i + 1 : N;
+            double mx = -INFINITY;
+            for (int32_t j = 0; j < N; ++j) prow[j] = 0.0;
+            for (int32_t j = 0; j < nk; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < d; ++c)
+                    acc += q[i * ts + (int64_t)h * d + c] * k[j * ts + (int64_t)h * d + c];
+                prow[j] = scale * acc;
+                if (prow[j] > mx) mx = prow[j];
+            }
+            double z = 0.0;
+            for (int32_t j = 0; j < nk; ++j) { prow[j] = exp(prow[j] - mx); z += prow[j]; }
+            for (int32_t j = 0; j < nk; ++j) prow[j] /= z;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Incoherent processing: random-sign diagonal times Hadamard matrix.        */
+/* ------------------------------------------------------------------------ */
+
+static int is_pow2(int32_t d) { return d > 0 && (d & (d - 1)) == 0; }
+
+static int popcount32(uint32_t x)
+{
+    int n = 0;
+    while (x) { n += (int)(x & 1u); x >>= 1; }
+    return n;
+}
+
+/* Sylvester Hadamard matrix H_d (entries +-1), row-major d x d. */
+int oracle_hadamard_matrix(int32_t d, double *hm)
+{
+    if (!hm || !is_pow2(d)) return -1;
+    for (int32_t i = 0; i < d; ++i)
+        for (int32_t j = 0; j < d; ++j)
+            hm[(int64_t)i * d + j] = (popcount32((uint32_t)(i & j)) & 1) ? -1.0 : 1.0;
+    return 0;
+}
+
+/*
+ * out_row = x_row * M with M = diag(signs) * H_d / sqrt(d), i.e.
+ * out[j] = sum_i x[i] * signs[i] * H[i][j] / sqrt(d), for every row of a
+ * row-major [nrows, d] array.  signs == NULL means D = I.
+ */
+int oracle_rotate(const double *x, int64_t nrows, int32_t d, const int8_t *signs, double *out)
+{
+    if (!x || !out || nrows < 0 || !is_pow2(d)) return -1;
+    double *hm = (double *)malloc(sizeof(double) * (size_t)d * (size_t)d);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!hm || !tmp) { free(hm); free(tmp); return -2; }
+    oracle_hadamard_matrix(d, hm);
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double *xr = x + r * d;
+        for (int32_t i = 0; i < d; ++i) tmp[i] = xr[i] * (signs ? (double)signs[i] : 1.0);
+        for (int32_t j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int32_t i = 0; i < d; ++i) acc += tmp[i] * hm[(int64_t)i * d + j];
+            out[r * d + j] = acc * inv_sqrt_d;
+        }
+    }
+    free(hm);
+    free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* e4m3 (OCP 8-bit floating point, E4M3 "FN": bias 7, no infinities,         */
+/* S.1111.111 is NaN, largest finite 448).                                   */
+/* ------------------------------------------------------------------------ */
+
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m, -9);                 /* m/8 * 2^(1-7) */
+    else mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Nearest e4m3 value, ties to the even code, saturating to +-448. */
+uint8_t oracle_e4m3_encode(double x)
+{
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* codes 0..126 are the non-negative finite values in increasing order:
+       find the largest code whose value does not exceed a. */
+    int lo = 0, hi = 126;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (oracle_e4m3_decode((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    int c = lo;
+    const double below = oracle_e4m3_decode((uint8_t)c);
+    if (below != a) {
+        const double above = oracle_e4m3_decode((uint8_t)(c + 1));
+        const double dlo = a - below, dhi = above - a;
+        if (dhi < dlo || (dhi == dlo && (c & 1))) c = c + 1;
+    }
+    return (uint8_t)(sign | c);
+}
+
+int oracle_e4m3_encode_array(const double *x, int64_t n, uint8_t *out)
+{
+    if (!x || !out || n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+    if (!c || !out || n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+    return 0;
+}
+
+/*
+ * Block quantisation of x [B, N, H, d] (already rotated for Q and K).
+ * Blocks are `block` consecutive tokens of one (b, h) over all d channels
+ * (the last block of a sequence may be partial); with per_tensor != 0 a
+ * single scale covers the whole tensor.  scale = amax(|x|)/448 (1 when the
+ * block is all zero); codes[i] = e4m3(x[i] / scale); descale[b][h][blk] =
+ * scale, so x ~ decode(code) * descale.
+ */
+int oracle_block_quant(const double *x, int32_t B, int32_t N, int32_t H, int32_t d,
+                       int32_t block, int32_t per_tensor, uint8_t *codes, double *descale)
+{
+    if (!x || !codes || !descale || B < 1 || N < 1 || H < 1 || d < 1 || block < 1) return -1;
+    const int32_t nblk = (N + block - 1) / block;
+    const int64_t ts = (int64_t)H * d;
+    double tensor_amax = 0.0;
+    if (per_tensor) {
+        const int64_t n = (int64_t)B * N * H * d;
+        for (int64_t i = 0; i < n; ++i) if (fabs(x[i]) > tensor_amax) tensor_amax = fabs(x[i]);
+    }
+    for (int32_t b = 0; b < B; ++b)
+        for (int32_t h = 0; h < H; ++h)
+            for (int32_t blk = 0; blk < nblk; ++blk) {
+                const int32_t t0 = blk * block;
+                const int32_t t1 = (t0 + block < N) ? t0 + block : N;
+                double amax = tensor_amax;
+                if (!per_tensor) {
+                    amax = 0.0;
+                    for (int32_t t = t0; t < t1; ++t)
+                        for (int32_t c = 0; c < d; ++c) {
+                            const double a = fabs(x[((int64_t)b * N + t) * ts + (int64_t)h * d + c]);
+                            if (a > amax) amax = a;
+                        }
+                }
+                const double scale = amax > 0.0 ? amax / 448.0 : 1.0;
+                descale[((int64_t)b * H + h) * nblk + blk] = scale;
+                for (int32_t t = t0; t < t1; ++t)
+                    for (int32_t c = 0; c < d; ++c) {
+                        const int64_t i = ((int64_t)b * N + t) * ts + (int64_t)h * d + c;
+                        codes[i] = oracle_e4m3_encode(x[i] / scale);
+                    }
+            }
+    return 0;
+}
