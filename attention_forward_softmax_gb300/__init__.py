@@ -1,0 +1,182 @@
+"""GB300 (sm_103a) fused attention forward: Python binding of libattn_gb300.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI (``include/attn.h``).  PyTorch supplies device
+memory and the current stream.  There is no CPU path: if the library is not
+built, every call raises.
+
+    o, lse = attn_fwd(q, k, v, causal=False)                       # [B,N,H,d]
+    o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen)      # [T,H,d]
+    q8, k8, v8, dq, dk, dv = qkv_block_quant_hadamard(q, k, v, signs)
+    o, lse = attn_fwd_fp8(q8, k8, v8, dq, dk, dv)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libattn_gb300.so")
+
+ATTN_BF16, ATTN_FP16 = 0, 1
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
+          6: "ATTN_ERR_BAD_SEQLENS", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_TOO_LARGE"}
+EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_fp8", "qkv_block_quant_hadamard",
+           "attn_get_status", "attn_status_string", "attn_shutdown", "attn_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built ({LIB_PATH} missing); "
+                                   "run attention_forward_softmax_gb300.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+            L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+            L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+            L.qkv_block_quant_hadamard.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i,
+                                                   i, i, i, i, vp]
+            L.attn_get_status.argtypes = [vp]
+            L.attn_status_string.argtypes = [i]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_version.restype = ctypes.c_uint32
+            for nm in EXPORTS[:5]:
+                getattr(L, nm).restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise AttnError(rc, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """Dense attention, q/k/v [B, N, H, d] bf16 or fp16 -> (o [B,N,H,d], lse [B,H,N] fp32)."""
+    _need_cuda(q, k, v)
+    B, N, H, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must have the same shape and dtype")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _need_cuda(o, lse)
+    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                        int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+                    stream=None):
+    """Packed attention, q/k/v [T, H, d], cu_seqlens int32 [nseq+1] on the device
+    -> (o [T,H,d], lse [H,T] fp32)."""
+    _need_cuda(q, k, v, cu_seqlens)
+    T, H, d = q.shape
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((H, T), device=q.device, dtype=torch.float32)
+    _need_cuda(o, lse)
+    rc = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                               cu_seqlens.numel() - 1, T, int(max_seqlen), H, d, scale,
+                               int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool = False,
+                 scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+                 stream=None):
+    """e4m3 attention: q8/k8/v8 [B,N,H,d] uint8 codes, descales fp32 [B,H,ceil(N/128)]
+    -> (o [B,N,H,d] bf16, lse [B,H,N] fp32)."""
+    _need_cuda(q8, k8, v8, descale_q, descale_k, descale_v)
+    B, N, H, d = q8.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty(q8.shape, device=q8.device, dtype=torch.bfloat16) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32)
+    _need_cuda(o, lse)
+    rc = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(descale_q), _ptr(descale_k),
+                            _ptr(descale_v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                            int(bool(causal)), _stream(stream))
+    _check(rc, "attn_fwd_fp8")
+    return o, lse
+
+
+def qkv_block_quant_hadamard(q, k, v, signs=None, per_tensor: bool = False, outs=None,
+                             stream=None):
+    """bf16 q/k/v [B,N,H,d] -> (q8, k8, v8 uint8 e4m3 codes, dq, dk, dv fp32 [B,H,nblk])."""
+    _need_cuda(q, k, v, signs)
+    B, N, H, d = q.shape
+    nblk = (N + 127) // 128
+    if outs is None:
+        outs = [torch.empty(q.shape, device=q.device, dtype=torch.uint8) for _ in range(3)] + \
+               [torch.empty((B, H, nblk), device=q.device, dtype=torch.float32) for _ in range(3)]
+    q8, k8, v8, dq, dk, dv = outs
+    rc = lib().qkv_block_quant_hadamard(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8),
+                                        _ptr(v8), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(signs),
+                                        int(bool(per_tensor)), B, H, N, d, _stream(stream))
+    _check(rc, "qkv_block_quant_hadamard")
+    return q8, k8, v8, dq, dk, dv
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word (0 = ok)."""
+    return int(lib().attn_get_status(_stream(stream)))
+
+
+def check_status(stream=None):
+    _check(get_status(stream), "device")

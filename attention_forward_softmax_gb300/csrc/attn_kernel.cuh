@@ -1,0 +1,561 @@
+// attn_kernel.cuh -- fused attention forward for sm_103a.
+//
+// What it computes ("Fused attention kernel", wikillm concept card, Overview
+// and Implementation sketch): for each query row, the running-softmax loop
+// over key blocks -- new row max, rescale factor exp(m_old - m_new) applied to
+// the running sum and the output, P = exp(S - m), O += P V -- then O / l and
+// lse = m + log l.  Every key block is scored (the card's note on the
+// printed loop bound), the rescale factor multiplies the OLD state (the
+// card's note on the inverted factor).
+//
+// How it is laid out on the GPU (our design, not the card's Hopper one):
+//  * one CTA per SM, persistent over work tiles; a work tile is 256 query
+//    rows of one (sequence, head), split into two 128-row sub-tiles A and B;
+//  * warp roles (320 threads):
+//      warps 0-3  softmax warpgroup for sub-tile A (one thread per row)
+//      warps 4-7  softmax warpgroup for sub-tile B
+//      warp  8    MMA issuer (one thread) + TMEM allocation
+//      warp  9    TMA producer (one thread)
+//  * Q sub-tiles stay in shared memory for the whole tile; K and V tiles of
+//    128 keys stream through a ring of NS slots (K_0, V_0, K_1, V_1, ...);
+//  * TMEM (512 columns): S_A [0,128), S_B [128,256), O_A, O_B after them;
+//    P (16-bit or e4m3) is written back over the first columns of its S;
+//  * tensor-core order per key block j:  S_A(j), O_B += P_B(j-1) V_{j-1},
+//    S_B(j), O_A += P_A(j) V_j -- so each softmax warpgroup works while the
+//    tensor core serves the other sub-tile.  A commit after S_X(j) also
+//    covers the earlier O_X update, so when softmax X sees S_X(j) ready its O
+//    is current and it may rescale O in place;
+//  * the output is rescaled only when a row max grows by more than
+//    kRescaleThresh (log2 units); otherwise the stale max is kept, which is
+//    exact after the final division by l;
+//  * every mbarrier wait is bounded (clock64 budget): on expiry the kernel
+//    records ATTN_ERR_TIMEOUT in the status word, drains its own copies and
+//    MMAs, frees TMEM and returns.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace attn {
+
+enum class Elem : int { BF16 = 0, F16 = 1, E4M3 = 2 };
+
+struct Params {
+  void *o;                  // output [B,N,H,d] or [T,H,d] (bf16/f16; bf16 for e4m3 inputs)
+  float *lse;               // [B,H,N] or [H,T]; may be null
+  const int *cu_seqlens;    // varlen: [nseq+1]
+  const int2 *tiles;        // varlen: (sequence, query-tile) in schedule order
+  const int *num_entries;   // varlen: number of valid entries in `tiles`
+  int B;                    // dense: batch; varlen: number of sequences
+  int H;
+  int N;                    // dense: sequence length; varlen: max sequence length
+  int T;                    // varlen: total tokens
+  int num_tiles;            // dense: exact count; varlen: upper bound
+  int causal;
+  float scale_log2;         // scale * log2(e)
+  const float *dq, *dk, *dv;  // e4m3: per-block descales [B,H,nblk]
+  int nblk;
+  long long wait_budget;
+  int *status;
+};
+
+template <int D_, Elem E_, bool Varlen_>
+struct Cfg {
+  static constexpr int D = D_;
+  static constexpr Elem E = E_;
+  static constexpr bool kVarlen = Varlen_;
+  static constexpr bool kFp8 = (E_ == Elem::E4M3);
+  static constexpr int kElt = kFp8 ? 1 : 2;
+  static constexpr int BM = 128;                       // rows per sub-tile
+  static constexpr int BN = 128;                       // keys per K/V tile
+  static constexpr int kRowBytes = D * kElt;           // one row of a tile
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static constexpr int kChunks = kRowBytes / 128;      // 128-byte column chunks per row
+  static constexpr int kChunkElems = 128 / kElt;
+  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 bytes
+  static constexpr int kTileBytes = 128 * kRowBytes;   // one Q sub-tile / K or V tile
+  static constexpr int kSmemBudget = 200 * 1024;
+  static constexpr int NS = (kSmemBudget - 2 * kTileBytes) / kTileBytes > 8
+                                ? 8
+                                : (kSmemBudget - 2 * kTileBytes) / kTileBytes;
+  static_assert(NS >= 3, "K/V ring too small");
+  // MMA shapes.  Each instruction consumes 32 bytes of K per row.
+  static constexpr int kKStep = 32 / kElt;             // 16 (16-bit) or 32 (e4m3)
+  static constexpr int kQKSteps = kRowBytes / 32;
+  static constexpr int kPVSteps = BN / kKStep;
+  static constexpr uint32_t kFmt = (E_ == Elem::BF16) ? 1u : 0u;
+  static constexpr uint32_t kIdescQK = idesc_make(kFmt, 128, BN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_make(kFmt, 128, D, false, true);
+  // TMEM columns
+  static constexpr uint32_t kColS = 128;              // S_X starts at column x * kColS
+  static constexpr uint32_t kColO0 = 256;
+  static constexpr int kPCols = BN * kElt / 4;         // 64 (16-bit P) or 32 (e4m3 P)
+  // Output rescale threshold in log2 units.  16-bit P may grow to 2^8 before
+  // a rescale; e4m3 P is stored as p * (256 * dv_j / dv_max) and must stay
+  // below 448, so there the threshold is log2(1.74).
+  static constexpr float kRescaleThresh = kFp8 ? 0.8f : 8.0f;
+  static constexpr int kThreads = 320;
+  // shared memory layout (offsets from the 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + NS * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NS + 8 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
+};
+
+struct TileInfo {
+  int b;          // dense batch index / varlen sequence index
+  int h;
+  int qt;         // query tile (256 rows) within the sequence
+  int L;          // sequence length
+  int start;      // first token of the sequence in the packed / flattened rows
+  int nA, nB;     // key tiles processed by sub-tiles A and B
+};
+
+template <class C>
+__device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, TileInfo &ti) {
+  if (t >= num_tiles) return false;
+  if constexpr (!C::kVarlen) {
+    const int nqt = (p.N + 255) / 256;
+    const int BH = p.B * p.H;
+    int bh;
+    if (p.causal) {   // heaviest query tiles first
+      ti.qt = nqt - 1 - t / BH;
+      bh = t % BH;
+    } else {          // neighbouring CTAs share one head's K/V in L2
+      bh = t / nqt;
+      ti.qt = t % nqt;
+    }
+    ti.b = bh / p.H;
+    ti.h = bh % p.H;
+    ti.L = p.N;
+    ti.start = ti.b * p.N;
+  } else {
+    const int2 e = p.tiles[t / p.H];
+    ti.h = t % p.H;
+    ti.b = e.x;
+    ti.qt = e.y;
+    ti.start = p.cu_seqlens[e.x];
+    ti.L = p.cu_seqlens[e.x + 1] - ti.start;
+  }
+  const int nkv = (ti.L + 127) / 128;
+  if (p.causal) {
+    ti.nA = min(2 * ti.qt + 1, nkv);
+    ti.nB = (ti.qt * 256 + 128 < ti.L) ? min(2 * ti.qt + 2, nkv) : ti.nA;
+  } else {
+    ti.nA = nkv;
+    ti.nB = nkv;
+  }
+  return true;
+}
+
+template <class C>
+__device__ __forceinline__ int tile_count(const Params &p) {
+  if constexpr (C::kVarlen) {
+    return min(p.num_tiles, __ldg(p.num_entries) * p.H);
+  } else {
+    return p.num_tiles;
+  }
+}
+
+// A wait that ignores the abort flag: used only to drain our own copies and
+// MMAs before the CTA exits.  Its budget is fixed (about two seconds) and
+// independent of the pipeline-wait budget, so even a run whose waits were
+// made to expire at once lets every copy and MMA land before exit.
+constexpr long long kDrainBudget = 1LL << 32;
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                long long budget = kDrainBudget) {
+  const uint32_t a = smem_addr(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > budget) return;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = smem + C::kOffQ;
+  uint8_t *sKV = smem + C::kOffKV;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *bar_q_full = bars + 0;
+  uint64_t *bar_q_empty = bars + 1;
+  uint64_t *bar_kv_full = bars + 2;
+  uint64_t *bar_kv_empty = bars + 2 + C::NS;
+  uint64_t *bar_s_full = bars + 2 + 2 * C::NS;     // [2]
+  uint64_t *bar_p_full = bar_s_full + 2;           // [2]
+  uint64_t *bar_o_final = bar_s_full + 4;          // [2]
+  uint64_t *bar_o_free = bar_s_full + 6;           // [2]
+  uint64_t *bar_drain = bar_s_full + 8;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&bar_kv_full[i], 1);
+      mbar_init(&bar_kv_empty[i], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s_full[x], 1);
+      mbar_init(&bar_p_full[x], 128);
+      mbar_init(&bar_o_final[x], 1);
+      mbar_init(&bar_o_free[x], 128);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl wc{abort_flag, p.status, p.wait_budget};
+  const int num_tiles = tile_count<C>(p);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------------
+    // TMA producer
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      int kv_pos = 0, tcount = 0, q_issued = 0;
+      bool ok = true;
+      TileInfo ti;
+      for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+        if (!mbar_wait(bar_q_empty, (tcount & 1) ^ 1, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar_q_full, 2 * C::kTileBytes);
+        ++q_issued;
+        for (int x = 0; x < 2; ++x) {
+          const int row = ti.qt * 256 + x * 128;
+          for (int c = 0; c < C::kChunks; ++c) {
+            uint8_t *dst = sQ + x * C::kTileBytes + c * C::kChunkBytes;
+            if constexpr (C::kVarlen)
+              tma_load_3d(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, ti.start + row);
+            else
+              tma_load_4d(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, row, ti.b);
+          }
+        }
+        for (int j = 0; ok && j < ti.nB; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++kv_pos) {
+            const int slot = kv_pos % C::NS;
+            const int round = kv_pos / C::NS;
+            if (!mbar_wait(&bar_kv_empty[slot], (round & 1) ^ 1, wc)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bar_kv_full[slot], C::kTileBytes);
+            const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
+            for (int c = 0; c < C::kChunks; ++c) {
+              uint8_t *dst = sKV + slot * C::kTileBytes + c * C::kChunkBytes;
+              if constexpr (C::kVarlen)
+                tma_load_3d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.h,
+                            ti.start + j * 128);
+              else
+                tma_load_4d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.h, j * 128, ti.b);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for the last copy issued into every slot and
+        // for the last Q copy, so no copy lands after the CTA has exited.
+        for (int i = 0; i < C::NS && i < kv_pos; ++i) {
+          const int pos = kv_pos - 1 - i;
+          mbar_wait_drain(&bar_kv_full[pos % C::NS], (pos / C::NS) & 1);
+        }
+        if (q_issued > 0) mbar_wait_drain(bar_q_full, (q_issued - 1) & 1);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------------
+    // MMA issuer
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t sQa = smem_addr(sQ);
+      const uint32_t sKVa = smem_addr(sKV);
+      int kv_pos = 0, tcount = 0;
+      int p_cnt[2] = {0, 0};
+      bool ok = true;
+      TileInfo ti;
+
+      // S_X = Q_X K^T  (K tile at ring position pos)
+      auto issue_qk = [&](int x, int pos) {
+        const uint32_t qa = sQa + x * C::kTileBytes;
+        const uint32_t ka = sKVa + (pos % C::NS) * C::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < C::kQKSteps; ++s) {
+          const uint32_t off = (s / 4) * C::kChunkBytes + (s % 4) * 32;
+          const uint64_t ad = sdesc_sw128(qa + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(ka + off, 16, 1024);
+          if constexpr (C::kFp8)
+            mma_f8_ss(tmem + x * C::kColS, ad, bd, C::kIdescQK, s > 0);
+          else
+            mma_f16_ss(tmem + x * C::kColS, ad, bd, C::kIdescQK, s > 0);
+        }
+      };
+      // O_X (+)= P_X V  (V tile at ring position pos)
+      auto issue_pv = [&](int x, int pos, bool accumulate) {
+        const uint32_t va = sKVa + (pos % C::NS) * C::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < C::kPVSteps; ++s) {
+          const uint64_t bd = sdesc_sw128(va + s * C::kKStep * 128, C::kChunkBytes, 1024);
+          const uint32_t pa = tmem + x * C::kColS + s * 8;
+          if constexpr (C::kFp8)
+            mma_f8_ts(tmem + C::kColO0 + x * C::D, pa, bd, C::kIdescPV, (accumulate || s > 0));
+          else
+            mma_f16_ts(tmem + C::kColO0 + x * C::D, pa, bd, C::kIdescPV, (accumulate || s > 0));
+        }
+      };
+      auto wait_kv = [&](int pos) {
+        if (!mbar_wait(&bar_kv_full[pos % C::NS], (pos / C::NS) & 1, wc)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto wait_p = [&](int x) {
+        if (!mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
+        ++p_cnt[x];
+        tc_fence_after();
+        return true;
+      };
+
+      for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+        const int nA = ti.nA, nB = ti.nB;
+        if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        for (int j = 0; j < nB; ++j) {
+          const int pk = kv_pos + 2 * j, pv = pk + 1;
+          if (!wait_kv(pk)) { ok = false; break; }
+          if (j < nA) {
+            issue_qk(0, pk);
+            mma_commit(&bar_s_full[0]);
+          }
+          if (j >= 1) {   // O_B (+)= P_B(j-1) V_{j-1}
+            if (!wait_p(1)) { ok = false; break; }
+            if (j - 1 == 0) {
+              if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+              tc_fence_after();
+            }
+            if (j - 1 >= nA && !wait_kv(pv - 2)) { ok = false; break; }
+            issue_pv(1, pv - 2, j - 1 > 0);
+            mma_commit(&bar_kv_empty[(pv - 2) % C::NS]);
+          }
+          issue_qk(1, pk);
+          mma_commit(&bar_s_full[1]);
+          mma_commit(&bar_kv_empty[pk % C::NS]);
+          if (j == nB - 1) mma_commit(bar_q_empty);
+          if (j < nA) {   // O_A (+)= P_A(j) V_j
+            if (!wait_p(0)) { ok = false; break; }
+            if (j == 0) {
+              if (!mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+              tc_fence_after();
+            }
+            if (!wait_kv(pv)) { ok = false; break; }
+            issue_pv(0, pv, j > 0);
+            if (j == nA - 1) mma_commit(&bar_o_final[0]);
+          }
+        }
+        if (!ok) break;
+        {   // O_B (+)= P_B(nB-1) V_{nB-1}
+          const int j = nB - 1;
+          const int pv = kv_pos + 2 * j + 1;
+          if (!wait_p(1)) { ok = false; break; }
+          if (j == 0) {
+            if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+            tc_fence_after();
+          }
+          if (j >= nA && !wait_kv(pv)) { ok = false; break; }
+          issue_pv(1, pv, j > 0);
+          mma_commit(&bar_o_final[1]);
+          mma_commit(&bar_kv_empty[pv % C::NS]);
+        }
+        kv_pos += 2 * nB;
+      }
+      // Drain every MMA this thread issued before TMEM is released.
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------
+    // Softmax warpgroups: x = 0 (sub-tile A) or 1 (sub-tile B)
+    // ------------------------------------------------------------------
+    const int x = warp >> 2;
+    const int wq = warp & 3;                 // TMEM lane quarter of this warp
+    const int r_in = wq * 32 + lane;         // row within the sub-tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + x * C::kColS;
+    const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
+    int s_cnt = 0, tcount = 0;
+    bool ok = true;
+    TileInfo ti;
+    for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+      const int nX = x == 0 ? ti.nA : ti.nB;
+      const int row0 = ti.qt * 256 + x * 128;          // first row of the sub-tile
+      const int row = row0 + r_in;                      // this thread's row
+      float m_run = -INFINITY;                          // running max, log2 units
+      float l_run = 0.f;
+      float pv_scale = 1.f;                             // e4m3: dv_max / 256
+      float dq_s = 0.f;
+      const float *dk_row = nullptr;
+      const float *dv_row = nullptr;
+      float inv_dv_max = 0.f;
+      if constexpr (C::kFp8) {
+        const size_t base = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
+        dq_s = __ldg(p.dq + base + (row0 >> 7));
+        dk_row = p.dk + base;
+        dv_row = p.dv + base;
+        float dvm = 0.f;
+        for (int i = 0; i < (ti.L + 127) / 128; ++i) dvm = fmaxf(dvm, __ldg(dv_row + i));
+        inv_dv_max = 256.f / dvm;
+        pv_scale = dvm / 256.f;
+      }
+      for (int j = 0; j < nX; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        // scale of this key block (log2 units per raw score)
+        float cs = p.scale_log2;
+        float pw = 1.f;                                   // e4m3: P prescale
+        if constexpr (C::kFp8) {
+          cs *= dq_s * __ldg(dk_row + j);
+          pw = __ldg(dv_row + j) * inv_dv_max;
+        }
+        const int kbase = j * 128;
+        const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
+        if (need_mask) {
+          const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kbase + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        const float m_tile = mx * cs;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool resc = m_new > m_run + C::kRescaleThresh;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m_run - m_new);    // 0 when m_run = -inf
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float rs = 0.f;
+        if constexpr (!C::kFp8) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), cs, -m_use));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), cs, -m_use));
+              rs += p0 + p1;
+              pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
+          }
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float q4[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                q4[u] = ex2(fmaf(__uint_as_float(sr[c][4 * i + u]), cs, -m_use));
+                rs += q4[u];
+              }
+              pk[c * 8 + i] = pack_e4m3x4(q4[0] * pw, q4[1] * pw, q4[2] * pw, q4[3] * pw);
+            }
+          tmem_st32(tS, pk);
+        }
+        l_run += rs;
+        tc_fence_before();
+        mbar_arrive(&bar_p_full[x]);
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O / l, lse ----------------
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_final[x], tcount & 1, wc))) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = row < ti.L;
+      const float inv_l = (l_run > 0.f) ? pv_scale / l_run : 0.f;
+      using OutT = uint32_t;
+      OutT *orow = nullptr;
+      if (valid) {
+        const size_t tok = static_cast<size_t>(ti.start) + row;
+        orow = reinterpret_cast<OutT *>(reinterpret_cast<uint8_t *>(p.o) +
+                                        ((tok * p.H + ti.h) * C::D) * 2);
+      }
+#pragma unroll
+      for (int c = 0; c < C::D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = __uint_as_float(o[2 * i]) * inv_l;
+            const float b = __uint_as_float(o[2 * i + 1]) * inv_l;
+            w[i] = (C::E == Elem::F16) ? pack_f16(a, b) : pack_bf16(a, b);
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && p.lse != nullptr) {
+        const float lse2 = m_run + __log2f(l_run);
+        const float lse = lse2 * 0.69314718055994531f;
+        if constexpr (C::kVarlen)
+          p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
+        else
+          p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.N + row] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_o_free[x]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn

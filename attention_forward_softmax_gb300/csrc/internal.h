@@ -1,0 +1,56 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Everything one attention launch needs (already validated).
+struct LaunchArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  int B, H, N, d, T;
+  float scale;
+  int causal;
+  const int *cu_seqlens;     // varlen
+  const int2 *tiles;         // varlen tile list (device)
+  const int *num_entries;    // varlen tile-list length (device)
+  int num_tiles;             // dense: exact; varlen: upper bound (x H)
+  const float *dq, *dk, *dv; // e4m3 descales
+  int *status;
+  long long budget;
+  int num_sms;
+};
+
+attn_status_t launch_attn_bf16(const LaunchArgs &a, bool varlen, cudaStream_t s);
+attn_status_t launch_attn_f16(const LaunchArgs &a, bool varlen, cudaStream_t s);
+attn_status_t launch_attn_e4m3(const LaunchArgs &a, cudaStream_t s);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).  dims/strides/box are innermost-first; strides has
+// rank-1 entries in bytes.
+attn_status_t encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr,
+                           const cuuint64_t *dims, const cuuint64_t *strides,
+                           const cuuint32_t *box, CUtensorMapSwizzle swizzle);
+
+// Per-device state.
+struct DeviceState {
+  int *status = nullptr;        // device status word
+  int *num_entries = nullptr;   // varlen tile-list length
+  float *scratch_amax = nullptr;  // per-tensor quantisation: 3 floats
+  int2 *tiles = nullptr;        // varlen tile list
+  size_t tiles_cap = 0;
+  int num_sms = 0;
+  unsigned attr_done = 0;       // bit per kernel instantiation: smem attribute set
+};
+attn_status_t device_state(DeviceState **out);
+attn_status_t ensure_tiles(DeviceState *ds, size_t entries);
+long long wait_budget();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace attn

@@ -1,0 +1,220 @@
+// quant.cu -- fp8 pre-step: incoherent processing and block quantisation
+// ("Fused attention kernel", wikillm concept card, section "8-bit forward
+// pass (FP8, Hopper)": one scale per block of Q, K and V; Q and K multiplied
+// by a random-sign diagonal times a Hadamard matrix before quantisation).
+//
+// One CTA per (tensor, batch, head, 128-token block).  Each warp owns 16
+// token rows; a row of d channels is spread over the 32 lanes (d/32
+// consecutive channels per lane).  For Q and K the row is multiplied by the
+// signs, then transformed by a fast Walsh-Hadamard transform (butterflies
+// inside a lane, then across lanes with shuffles), then scaled by 1/sqrt(d);
+// this equals x * diag(s) * H_d / sqrt(d) with H_d the Sylvester matrix.
+// The block's amax is reduced through shared memory, scale = amax / 448, and
+// every value is divided by the scale and rounded to e4m3 (nearest even,
+// saturating).  HBM-bound: 2 bytes read and 1 byte written per element.
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kQThreads = 256;
+constexpr int kRowsPerWarp = 16;
+
+struct QuantArgs {
+  const __nv_bfloat16 *x[3];
+  uint8_t *y[3];
+  float *descale[3];
+  const int8_t *signs;   // may be null
+  int B, H, N, nblk;
+  int mode;              // 0: block scales; 1: amax only (per-tensor pass 1); 2: quantise with
+                         //    the per-tensor scale in tensor_amax (pass 2)
+  const float *tensor_amax;  // [3], mode 2
+};
+
+template <int D>
+__global__ void __launch_bounds__(kQThreads)
+    quant_kernel(const QuantArgs a) {
+  constexpr int EPL = D / 32;   // channels per lane
+  const int tensor = blockIdx.z;
+  const int bh = blockIdx.y;
+  const int blk = blockIdx.x;
+  const int b = bh / a.H, h = bh % a.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool rotate = (tensor < 2) && (a.signs != nullptr);
+  __shared__ float red[kQThreads / 32];
+
+  float sg[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) sg[e] = rotate ? static_cast<float>(a.signs[lane * EPL + e]) : 1.f;
+
+  const __nv_bfloat16 *xin = a.x[tensor];
+  const int t0 = blk * 128 + warp * kRowsPerWarp;
+  float v[kRowsPerWarp][EPL];
+  float amax = 0.f;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int t = t0 + r;
+    if (t < a.N) {
+      const size_t off = ((static_cast<size_t>(b) * a.N + t) * a.H + h) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(xin + off);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+        v[r][0] = __low2float(p0);
+        v[r][1] = __high2float(p0);
+        v[r][2] = __low2float(p1);
+        v[r][3] = __high2float(p1);
+      } else {
+        const uint32_t raw = *reinterpret_cast<const uint32_t *>(xin + off);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        v[r][0] = __low2float(p0);
+        v[r][1] = __high2float(p0);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[r][e] = 0.f;
+    }
+  }
+  if (rotate) {
+    const float norm = 1.f / sqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[r][e] *= sg[e];
+      // butterflies between channels of one lane (strides 1, 2, ...)
+#pragma unroll
+      for (int hs = 1; hs < EPL; hs <<= 1)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          if ((e & hs) == 0) {
+            const float u = v[r][e], w = v[r][e + hs];
+            v[r][e] = u + w;
+            v[r][e + hs] = u - w;
+          }
+      // butterflies across lanes (channel stride EPL * m)
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, v[r][e], m);
+          v[r][e] = upper ? (other - v[r][e]) : (v[r][e] + other);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[r][e] *= norm;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  float bmax = 0.f;
+#pragma unroll
+  for (int w = 0; w < kQThreads / 32; ++w) bmax = fmaxf(bmax, red[w]);
+
+  const size_t dslot = (static_cast<size_t>(b) * a.H + h) * a.nblk + blk;
+  if (a.mode == 1) {
+    if (threadIdx.x == 0) a.descale[tensor][dslot] = bmax;
+    return;
+  }
+  const float amx = (a.mode == 2) ? a.tensor_amax[tensor] : bmax;
+  const float scale = amx > 0.f ? amx / 448.f : 1.f;
+  if (threadIdx.x == 0) a.descale[tensor][dslot] = scale;
+  uint8_t *yout = a.y[tensor];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int t = t0 + r;
+    if (t >= a.N) break;
+    const size_t off = ((static_cast<size_t>(b) * a.N + t) * a.H + h) * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t *>(yout + off) =
+          pack_e4m3x4(__fdiv_rn(v[r][0], scale), __fdiv_rn(v[r][1], scale),
+                      __fdiv_rn(v[r][2], scale), __fdiv_rn(v[r][3], scale));
+    } else {
+      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[r][0], scale), __fdiv_rn(v[r][1], scale), 0.f, 0.f);
+      *reinterpret_cast<uint16_t *>(yout + off) = static_cast<uint16_t>(w & 0xFFFFu);
+    }
+  }
+}
+
+// Per-tensor pass between the two quantisation passes: max over the block
+// amaxes of each tensor.
+__global__ void tensor_amax_kernel(const float *dq, const float *dk, const float *dv, int n,
+                                   float *out) {
+  const float *src = blockIdx.x == 0 ? dq : (blockIdx.x == 1 ? dk : dv);
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, src[i]);
+  __shared__ float red[32];
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+    out[blockIdx.x] = r;
+  }
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void *v,
+                                                  void *q8, void *k8, void *v8,
+                                                  float *descale_q, float *descale_k,
+                                                  float *descale_v, const int8_t *signs,
+                                                  int per_tensor, int B, int H, int N, int d,
+                                                  void *stream) {
+  if (!q || !k || !v || !q8 || !k8 || !v8 || !descale_q || !descale_k || !descale_v)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(v8))
+    return ATTN_ERR_MISALIGNED;
+  const long long nblk = (N + 127) / 128;
+  if (static_cast<long long>(B) * H > 65535 || nblk > 0x7fffffff ||
+      static_cast<long long>(B) * N * H * d > (1LL << 40))
+    return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  attn_status_t st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  QuantArgs a{};
+  a.x[0] = static_cast<const __nv_bfloat16 *>(q);
+  a.x[1] = static_cast<const __nv_bfloat16 *>(k);
+  a.x[2] = static_cast<const __nv_bfloat16 *>(v);
+  a.y[0] = static_cast<uint8_t *>(q8);
+  a.y[1] = static_cast<uint8_t *>(k8);
+  a.y[2] = static_cast<uint8_t *>(v8);
+  a.descale[0] = descale_q;
+  a.descale[1] = descale_k;
+  a.descale[2] = descale_v;
+  a.signs = signs;
+  a.B = B; a.H = H; a.N = N; a.nblk = static_cast<int>(nblk);
+  a.tensor_amax = ds->scratch_amax;
+  const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(B * H), 3);
+  auto run = [&](int mode) {
+    a.mode = mode;
+    if (d == 128) quant_kernel<128><<<grid, kQThreads, 0, s>>>(a);
+    else quant_kernel<64><<<grid, kQThreads, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess;
+  };
+  if (!per_tensor) return run(0) ? ATTN_OK : ATTN_ERR_LAUNCH;
+  if (!run(1)) return ATTN_ERR_LAUNCH;
+  tensor_amax_kernel<<<3, 1024, 0, s>>>(descale_q, descale_k, descale_v,
+                                        static_cast<int>(B * H * nblk), ds->scratch_amax);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return run(2) ? ATTN_OK : ATTN_ERR_LAUNCH;
+}

@@ -1,0 +1,294 @@
+// runtime.cu -- host side of the C ABI: argument validation, per-device
+// workspace and status word, tensor-map encoding, the varlen tile-list
+// builder, and the attn_fwd / attn_fwd_varlen / attn_fwd_fp8 entry points.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+
+namespace attn {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+}  // namespace
+
+long long wait_budget() {
+  static long long b = [] {
+    const char *e = std::getenv("ATTN_WAIT_BUDGET_CYCLES");
+    long long v = e ? std::atoll(e) : 0;
+    return v > 0 ? v : (1LL << 31);   // about one second at 2 GHz
+  }();
+  return b;
+}
+
+attn_status_t device_state(DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState &ds = g_dev[dev];
+  if (ds.status == nullptr) {
+    if (cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemset(p, 0, 256) != cudaSuccess) return ATTN_ERR_CUDA;
+    ds.status = static_cast<int *>(p);
+    ds.num_entries = ds.status + 1;
+    ds.scratch_amax = reinterpret_cast<float *>(ds.status + 4);
+  }
+  *out = &ds;
+  return ATTN_OK;
+}
+
+attn_status_t ensure_tiles(DeviceState *ds, size_t entries) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (ds->tiles_cap >= entries) return ATTN_OK;
+  size_t cap = ds->tiles_cap ? ds->tiles_cap : 4096;
+  while (cap < entries) cap *= 2;
+  if (ds->tiles) {
+    // The old list may still be read by queued work: wait before freeing.
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaFree(ds->tiles);
+    ds->tiles = nullptr;
+    ds->tiles_cap = 0;
+  }
+  void *p = nullptr;
+  if (cudaMalloc(&p, cap * sizeof(int2)) != cudaSuccess) return ATTN_ERR_CUDA;
+  ds->tiles = static_cast<int2 *>(p);
+  ds->tiles_cap = cap;
+  return ATTN_OK;
+}
+
+attn_status_t encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr,
+                           const cuuint64_t *dims, const cuuint64_t *strides,
+                           const cuuint32_t *box, CUtensorMapSwizzle swizzle) {
+  if (g_encode == nullptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+    }
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+// ---------------------------------------------------------------------------
+// Varlen schedule: validate cu_seqlens and list the (sequence, query-tile)
+// work tiles heaviest first (counting sort on the number of key tiles the
+// tile's heavier sub-tile scores).  One CTA; the list length goes to
+// *num_entries (0 when cu_seqlens is malformed, which is also reported in
+// the status word).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int tile_work(int L, int qt, int causal) {
+  const int nkv = (L + 127) / 128;
+  if (!causal) return nkv;
+  return (qt * 256 + 128 < L) ? min(2 * qt + 2, nkv) : min(2 * qt + 1, nkv);
+}
+
+constexpr int kSchedThreads = 1024;
+constexpr int kMaxWorkKey = 4096;
+
+__global__ void __launch_bounds__(kSchedThreads)
+    varlen_schedule_kernel(const int *cu, int nseq, int T, int max_seqlen, int causal, int2 *tiles,
+                           int capacity, int *num_entries, int *status) {
+  __shared__ int hist[kMaxWorkKey];
+  __shared__ int bad;
+  const int nkeys = min(kMaxWorkKey, (max_seqlen + 127) / 128 + 1);
+  if (threadIdx.x == 0) bad = 0;
+  for (int i = threadIdx.x; i < nkeys; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int a = cu[s], b = cu[s + 1];
+    if ((s == 0 && a != 0) || b < a || b - a > max_seqlen || (s == nseq - 1 && b != T)) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      *num_entries = 0;
+      atomicCAS(status, 0, 6 /* ATTN_ERR_BAD_SEQLENS */);
+    }
+    return;
+  }
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu[s + 1] - cu[s];
+    for (int qt = 0; qt * 256 < L; ++qt) atomicAdd(&hist[min(tile_work(L, qt, causal), nkeys - 1)], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {   // exclusive offsets, heaviest key first
+    int run = 0;
+    for (int k = nkeys - 1; k >= 0; --k) {
+      const int c = hist[k];
+      hist[k] = run;
+      run += c;
+    }
+    *num_entries = min(run, capacity);
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu[s + 1] - cu[s];
+    for (int qt = 0; qt * 256 < L; ++qt) {
+      const int pos = atomicAdd(&hist[min(tile_work(L, qt, causal), nkeys - 1)], 1);
+      if (pos < capacity) tiles[pos] = make_int2(s, qt);
+    }
+  }
+}
+
+namespace {
+
+attn_status_t check_common(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, int H, int d, float scale) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (H < 1 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int H, int N, int d, float scale, int causal, attn_dtype_t dtype,
+                       void *stream) {
+  attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  const long long tokens = static_cast<long long>(B) * N;
+  const long long tiles = static_cast<long long>(B) * H * ((N + 255) / 256);
+  if (tokens * H * d > (1LL << 40) || tiles > (1LL << 30)) return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  LaunchArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.N = N; a.d = d; a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
+  a.scale = scale; a.causal = causal ? 1 : 0;
+  a.num_tiles = static_cast<int>(tiles);
+  a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return dtype == ATTN_BF16 ? launch_attn_bf16(a, false, s) : launch_attn_f16(a, false, s);
+}
+
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int nseq, int total_tokens,
+                              int max_seqlen, int H, int d, float scale, int causal,
+                              attn_dtype_t dtype, void *stream) {
+  attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (!cu_seqlens || nseq < 1 || total_tokens < 1 || max_seqlen < 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return ATTN_ERR_MISALIGNED;
+  const long long entries = static_cast<long long>(total_tokens) / 256 + nseq;
+  if (static_cast<long long>(total_tokens) * H * d > (1LL << 40) || entries * H > (1LL << 30))
+    return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  if ((st = ensure_tiles(ds, static_cast<size_t>(entries))) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  varlen_schedule_kernel<<<1, kSchedThreads, 0, s>>>(cu_seqlens, nseq, total_tokens, max_seqlen,
+                                                     causal ? 1 : 0, ds->tiles,
+                                                     static_cast<int>(entries), ds->num_entries,
+                                                     ds->status);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  LaunchArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = nseq; a.H = H; a.N = max_seqlen; a.d = d; a.T = total_tokens;
+  a.scale = scale; a.causal = causal ? 1 : 0;
+  a.cu_seqlens = cu_seqlens; a.tiles = ds->tiles; a.num_entries = ds->num_entries;
+  a.num_tiles = static_cast<int>(entries * H);
+  a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  return dtype == ATTN_BF16 ? launch_attn_bf16(a, true, s) : launch_attn_f16(a, true, s);
+}
+
+attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *descale_q,
+                           const float *descale_k, const float *descale_v, void *o, float *lse,
+                           int B, int H, int N, int d, float scale, int causal, void *stream) {
+  attn_status_t st = check_common(q8, k8, v8, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (B < 1 || N < 1 || !descale_q || !descale_k || !descale_v) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long tokens = static_cast<long long>(B) * N;
+  const long long tiles = static_cast<long long>(B) * H * ((N + 255) / 256);
+  if (tokens * H * d > (1LL << 40) || tiles > (1LL << 30)) return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  LaunchArgs a{};
+  a.q = q8; a.k = k8; a.v = v8; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.N = N; a.d = d; a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
+  a.scale = scale; a.causal = causal ? 1 : 0;
+  a.num_tiles = static_cast<int>(tiles);
+  a.dq = descale_q; a.dk = descale_k; a.dv = descale_v;
+  a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  return launch_attn_e4m3(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_get_status(void *stream) {
+  DeviceState *ds = nullptr;
+  attn_status_t st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (h != 0 && cudaMemset(ds->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return static_cast<attn_status_t>(h);
+}
+
+const char *attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case ATTN_ERR_LAUNCH: return "kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_TOO_LARGE: return "problem size exceeds the supported index range";
+  }
+  return "unknown status";
+}
+
+void attn_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState &ds = g_dev[d];
+    if (ds.status == nullptr && ds.tiles == nullptr) continue;
+    if (cudaSetDevice(d) != cudaSuccess) continue;
+    cudaDeviceSynchronize();
+    if (ds.tiles) cudaFree(ds.tiles);
+    if (ds.status) cudaFree(ds.status);
+    ds = DeviceState{};
+  }
+  cudaSetDevice(cur);
+}
+
+uint32_t attn_version(void) { return 0x00000100u; }
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libattn_gb300.so).
+ *
+ * The operation is the fused scaled-dot-product attention forward pass,
+ * "Fused attention kernel" (wikillm concept card), Overview and
+ * Implementation sketch:
+ *
+ *     S = scale * Q K^T            (per batch entry / sequence and head)
+ *     P = softmax(S) row by row    (causal: query i sees keys j <= i)
+ *     O = P V,   lse_i = log sum_j exp(S_ij)   (natural log)
+ *
+ * computed tile by tile with a running row maximum and row sum so that S and
+ * P never leave the chip.  The 8-bit variant and its pre-step follow the same
+ * card's section "8-bit forward pass (FP8, Hopper)": e4m3 operands, one scale
+ * per block of Q, K and V, and Q, K rotated by a random-sign diagonal times a
+ * Hadamard matrix ("incoherent processing").
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *    where stated.  Buffers must not overlap.  Tensor pointers must be 16-byte
+ *    aligned (they are read and written by the Tensor Memory Accelerator).
+ *  - Layouts are row-major and contiguous:
+ *        dense  Q, K, V, O : [B, N, H, d]  (token-major, head dim innermost)
+ *        dense  lse        : [B, H, N] float32
+ *        varlen Q, K, V, O : [T, H, d]     (sequences packed back to back)
+ *        varlen lse        : [H, T] float32
+ *  - Supported head dimensions: d = 64 and d = 128.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call is asynchronous on that stream; the return value reports
+ *    argument validation and launch errors only.  Errors detected on the
+ *    device (a pipeline wait that timed out, malformed cu_seqlens) are
+ *    recorded in a device status word read by attn_get_status().
+ *  - No call throws, prints, or synchronises (except attn_get_status).
+ *  - The library keeps a small per-device workspace (status word, tile list),
+ *    allocated on first use and released by attn_shutdown().  Calls that share
+ *    a device must be issued from one host thread at a time or be serialised
+ *    by the caller.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, non-finite scale */
+    ATTN_ERR_UNSUPPORTED = 2,   /* head dimension or dtype this build does not provide */
+    ATTN_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_LAUNCH = 4,        /* the kernel launch failed */
+    ATTN_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded its budget */
+    ATTN_ERR_BAD_SEQLENS = 6,   /* device: cu_seqlens not non-decreasing from 0 or over total */
+    ATTN_ERR_CUDA = 7,          /* a CUDA runtime call failed (no device, out of memory) */
+    ATTN_ERR_TOO_LARGE = 8      /* a size exceeds the library's index range */
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
+
+/*
+ * Dense attention forward, 16-bit inputs.
+ *   q, k, v : [B, N, H, d] in `dtype`;  o : [B, N, H, d] in `dtype`;
+ *   lse     : [B, H, N] float32 (may be NULL: not written).
+ *   scale   : multiplies Q K^T (normally 1/sqrt(d)); must be finite.
+ *   causal  : nonzero = query i attends to keys 0..i of its own sequence.
+ * The result matches exact attention; S and P stay on chip.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int H, int N, int d, float scale, int causal,
+                       attn_dtype_t dtype, void *stream);
+
+/*
+ * Packed variable-length attention forward ("Varlen", named among the
+ * features of the HippoAttention case study, streamhpc.com).
+ *   cu_seqlens   : DEVICE int32 [nseq + 1]; sequence s occupies tokens
+ *                  cu_seqlens[s] .. cu_seqlens[s+1]-1; cu_seqlens[0] = 0,
+ *                  non-decreasing, cu_seqlens[nseq] = total_tokens.
+ *   total_tokens : T, the packed length (host value).
+ *   max_seqlen   : an upper bound on every sequence length (host value).
+ *   q, k, v, o   : [T, H, d];  lse : [H, T] float32 (may be NULL).
+ * Attention never crosses a sequence boundary.  A violated cu_seqlens
+ * contract is reported as ATTN_ERR_BAD_SEQLENS by attn_get_status() and the
+ * outputs are then unspecified.
+ */
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int nseq, int total_tokens,
+                              int max_seqlen, int H, int d, float scale, int causal,
+                              attn_dtype_t dtype, void *stream);
+
+/*
+ * 8-bit attention forward (e4m3 operands, block scales).
+ *   q8, k8, v8 : [B, N, H, d] e4m3 codes (uint8 storage), as produced by
+ *                qkv_block_quant_hadamard (Q and K possibly rotated: the
+ *                rotation cancels in Q K^T).
+ *   descale_q/k/v : float32 [B, H, ceil(N/128)]; block j of (b, h) covers
+ *                tokens 128j .. 128j+127 and dequantises as code * descale.
+ *   o   : [B, N, H, d] bf16;  lse : [B, H, N] float32 (may be NULL).
+ * V is consumed in its stored [token, d] layout (no transpose in memory).
+ */
+attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8,
+                           const float *descale_q, const float *descale_k,
+                           const float *descale_v, void *o, float *lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           void *stream);
+
+/*
+ * fp8 pre-step: incoherent processing and block quantisation.
+ *   q, k, v    : [B, N, H, d] bf16 inputs.
+ *   signs      : DEVICE int8 [d] of +1/-1 (the random sign diagonal D), or
+ *                NULL for no rotation.  Q and K are replaced by
+ *                x * D * H_d / sqrt(d) (H_d: Sylvester Hadamard matrix); V is
+ *                not rotated.
+ *   per_tensor : 0 = one scale per 128-token block of each (b, h);
+ *                1 = one scale per tensor (the baseline the block scheme is
+ *                compared against).
+ *   outputs    : q8, k8, v8 [B, N, H, d] e4m3; descale_q/k/v [B, H, ceil(N/128)]
+ *                float32 with scale = amax|x| / 448 (1 for an all-zero block),
+ *                codes = round-to-nearest-even(x / scale), saturated to +-448.
+ */
+attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void *v,
+                                       void *q8, void *k8, void *v8,
+                                       float *descale_q, float *descale_k, float *descale_v,
+                                       const int8_t *signs, int per_tensor,
+                                       int B, int H, int N, int d, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device (ATTN_OK if no device-side error was recorded since the
+ * last call).  Returns ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status_t attn_get_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/* Releases the per-device workspaces.  Safe to call more than once. */
+void attn_shutdown(void);
+
+/* Library ABI version: 0x00MMmmpp. */
+uint32_t attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,169 @@
+"""GPU parity of the 16-bit attention path (dense and varlen) against the
+fp64 oracle, element by element, on seeded inputs that span several tiles
+and a ragged tail; plus exactness of masking and the device status word."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_softmax_gb300 as agb
+import oracle
+from datagen import normal, to_bf16
+from tests._gpu_helpers import (assert_close_lse, assert_close_o, qkv, threads)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    agb.build()
+    agb.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_dense(q, k, v, causal, scale=None):
+    o, lse = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert agb.get_status() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 128, 129, 255, 256, 300, 513])
+def test_dense_parity_small(N, causal, d, dtype):
+    B, H = 2, 3
+    q, k, v = qkv(2000 + N + d, (B, N, H, d), dtype)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_dense(q, k, v, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal, nthreads=threads())
+    assert_close_o(o, o_ref, dtype, f"N={N} d={d} causal={causal}")
+    assert_close_lse(lse, lse_ref, f"N={N} d={d} causal={causal}")
+
+
+def test_tiny_config_b1_h1_n128_d64():
+    """bf16 non-causal attention fwd, B=1, H=1, N=128, d=64, scale=1/sqrt(d)."""
+    from datagen.workloads import TINY, make_inputs
+    x = make_inputs(TINY)
+    o, lse = run_dense(x["q"], x["k"], x["v"], False)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], TINY.scale, False)
+    assert_close_o(o, o_ref, torch.bfloat16, "tiny")
+    assert_close_lse(lse, lse_ref, "tiny")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_multi_tile_persistent(d, causal):
+    """More work tiles than SMs, so every CTA loops over several tiles."""
+    B, H, N = 3, 64, 600
+    q, k, v = qkv(2100 + d, (B, N, H, d), torch.bfloat16)
+    o, lse = run_dense(q, k, v, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), causal, nthreads=threads())
+    assert_close_o(o, o_ref, torch.bfloat16, "multi-tile")
+    assert_close_lse(lse, lse_ref, "multi-tile")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_parity(causal, d):
+    H = 4
+    lens = [1, 130, 77, 256, 513, 3, 300]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v = qkv(2200 + d, (T, H, d), torch.bfloat16)
+    cu_d = torch.from_numpy(cu).cuda()
+    o, lse = agb.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_d, max(lens), causal=causal)
+    torch.cuda.synchronize()
+    assert agb.get_status() == 0
+    o_ref, lse_ref = oracle.attention_varlen(q, k, v, cu, 1 / math.sqrt(d), causal,
+                                             nthreads=threads())
+    assert_close_o(o.float().cpu().numpy(), o_ref, torch.bfloat16, "varlen")
+    assert_close_lse(lse.cpu().numpy(), lse_ref, "varlen")
+
+
+def test_causal_future_keys_are_exactly_masked():
+    """Poison every key/value at or beyond row r (K = NaN / +-Inf, V = +-3e4):
+    outputs of rows < r must be bitwise identical to the clean run."""
+    B, N, H, d, r = 2, 400, 2, 128, 190
+    q, k, v = qkv(2300, (B, N, H, d), torch.bfloat16)
+    o1, l1 = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    kp, vp = k.clone(), v.clone()
+    kp[:, r:] = float("nan")
+    kp[:, r::3] = float("inf")
+    kp[:, r + 1::3] = float("-inf")
+    vp[:, r:] = 3e4
+    vp[:, r::2] = -3e4
+    o2, l2 = agb.attn_fwd(q.cuda(), kp.cuda(), vp.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :r].view(torch.int16), o2[:, :r].view(torch.int16))
+    assert torch.equal(l1[:, :, :r].view(torch.int32), l2[:, :, :r].view(torch.int32))
+
+
+def test_varlen_neighbours_are_exactly_masked():
+    """Poison every other sequence: each sequence's outputs are bitwise equal
+    to the clean run."""
+    H, d = 2, 128
+    lens = [70, 300, 129, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v = qkv(2400, (T, H, d), torch.bfloat16)
+    cu_d = torch.from_numpy(cu).cuda()
+    for causal in (False, True):
+        o1, l1 = agb.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_d, max(lens), causal=causal)
+        for s in range(len(lens)):
+            a, b = int(cu[s]), int(cu[s + 1])
+            kp, vp = k.clone(), v.clone()
+            kp[:a] = float("nan")
+            kp[b:] = float("nan")
+            vp[:a] = 3e4
+            vp[b:] = -3e4
+            o2, l2 = agb.attn_fwd_varlen(q.cuda(), kp.cuda(), vp.cuda(), cu_d, max(lens),
+                                         causal=causal)
+            torch.cuda.synchronize()
+            assert torch.equal(o1[a:b].view(torch.int16), o2[a:b].view(torch.int16)), (causal, s)
+            assert torch.equal(l1[:, a:b].view(torch.int32), l2[:, a:b].view(torch.int32))
+
+
+def test_dense_batches_are_independent():
+    """Poisoning batch entry 1 leaves batch entry 0 bitwise unchanged."""
+    B, N, H, d = 2, 200, 2, 64
+    q, k, v = qkv(2500, (B, N, H, d), torch.bfloat16)
+    o1, _ = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda())
+    kp, vp = k.clone(), v.clone()
+    kp[1] = float("nan")
+    vp[1] = 3e4
+    o2, _ = agb.attn_fwd(q.cuda(), kp.cuda(), vp.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(o1[0].view(torch.int16), o2[0].view(torch.int16))
+
+
+def test_deterministic():
+    B, N, H, d = 2, 777, 4, 128
+    q, k, v = [t.cuda() for t in qkv(2600, (B, N, H, d), torch.bfloat16)]
+    o1, l1 = agb.attn_fwd(q, k, v, causal=True)
+    o2, l2 = agb.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_lse_optional_and_custom_scale():
+    B, N, H, d = 1, 100, 2, 64
+    q, k, v = qkv(2700, (B, N, H, d), torch.bfloat16)
+    o, lse = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=0.3, want_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    o_ref, _ = oracle.attention(q, k, v, 0.3, False)
+    assert_close_o(o.float().cpu().numpy(), o_ref, torch.bfloat16, "scale 0.3")
+
+
+def test_malformed_cu_seqlens_reported():
+    H, d = 1, 64
+    q = torch.zeros((40, H, d), dtype=torch.bfloat16, device="cuda")
+    bad = torch.tensor([0, 30, 20, 40], dtype=torch.int32, device="cuda")   # decreasing
+    agb.attn_fwd_varlen(q, q, q, bad, 40)
+    assert agb.get_status() == 6
+    assert agb.get_status() == 0       # cleared by the read

@@ -1,0 +1,35 @@
+"""Failure detection without a GPU fault: with a one-cycle wait budget the
+kernel's pipeline waits expire at once; it must record ATTN_ERR_TIMEOUT,
+drain its own copies and MMAs, free TMEM and return, leaving the CUDA
+context usable.  Runs in a child process (the budget is read once per
+process from ATTN_WAIT_BUDGET_CYCLES)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import torch
+import attention_forward_softmax_gb300 as agb
+q = torch.randn(2, 2048, 8, 128, device="cuda").to(torch.bfloat16)
+agb.attn_fwd(q, q, q, causal=True)
+print("STATUS", agb.get_status())
+print("AGAIN", agb.get_status())
+x = torch.ones(16, device="cuda")
+print("CTX", float(x.sum()))
+"""
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    env = dict(os.environ, ATTN_WAIT_BUDGET_CYCLES="1", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", CHILD], env=env, capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    assert "STATUS 5" in r.stdout, r.stdout
+    assert "AGAIN 0" in r.stdout, r.stdout
+    assert "CTX 16.0" in r.stdout, r.stdout
