@@ -14,18 +14,25 @@ TOL_O = 2e-3
 TOL_LSE = 1e-3
 
 
-def ulp_half(x: np.ndarray, mant_bits: int) -> np.ndarray:
-    """Half a unit in the last place of |x| in a format with `mant_bits`
-    explicit mantissa bits (bf16: 7, fp16: 10)."""
-    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -14)))
-    return 2.0 ** (e - mant_bits) / 2
+def rel_round(dtype) -> float:
+    """Unit roundoff of round-to-nearest in the 16-bit type P and O are
+    stored in: 2^-p for p significant bits (bf16: 8, fp16: 11)."""
+    return 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -11
 
 
-def o_tolerance(o_ref: np.ndarray, dtype) -> np.ndarray:
-    """2e-3, plus the output format's own half-ulp where |O| is large enough
-    for rounding to exceed it (small N, where O is close to one V row)."""
-    bits = 7 if dtype == torch.bfloat16 else 10
-    return TOL_O + ulp_half(o_ref, bits)
+def o_tolerance(o_ref: np.ndarray, a_ref: np.ndarray, dtype) -> np.ndarray:
+    """Per-element bound on |O_gpu - O|.
+
+    The kernel rounds each probability p_k to the 16-bit type before the P V
+    product (relative error <= r) while the row sum l uses the fp32 p_k, so
+    O_gpu = sum_k w_k (1 + e_k) v_k with |e_k| <= r, i.e. an error of at most
+    r * sum_k w_k |v_k| = r * a_ref (a_ref: the oracle's attention output on
+    |V|), plus the final rounding of O (<= r |O|).  The tolerance is the
+    method's 2e-3 bar, or this bound (+1e-5 for fp32 accumulation and the
+    exp2 approximation) where the formats alone can exceed 2e-3 -- rows that
+    average only a few keys."""
+    r = rel_round(dtype)
+    return np.maximum(TOL_O, r * (np.abs(a_ref) + np.abs(o_ref)) + 1e-5)
 
 
 def qkv(seed, shape, dtype):
@@ -52,8 +59,8 @@ def max_err(a, b):
     return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
 
 
-def assert_close_o(o_gpu: np.ndarray, o_ref: np.ndarray, dtype, what=""):
-    tol = o_tolerance(o_ref, dtype)
+def assert_close_o(o_gpu: np.ndarray, o_ref: np.ndarray, a_ref: np.ndarray, dtype, what=""):
+    tol = o_tolerance(o_ref, a_ref, dtype)
     err = np.abs(o_gpu.astype(np.float64) - o_ref)
     bad = err > tol
     assert not bad.any(), (f"{what}: {bad.sum()} elements over tolerance; max err "
@@ -63,3 +70,16 @@ def assert_close_o(o_gpu: np.ndarray, o_ref: np.ndarray, dtype, what=""):
 def assert_close_lse(lse_gpu, lse_ref, what=""):
     err = max_err(lse_gpu, lse_ref)
     assert err <= TOL_LSE, f"{what}: max |dLSE| {err:.3e}"
+
+
+def oracle_dense(q, k, v, scale, causal):
+    """(O, lse, A) where A is the oracle output on |V| (for the tolerance)."""
+    o, lse = oracle.attention(q, k, v, scale, causal, nthreads=threads())
+    a, _ = oracle.attention(q, k, v.abs(), scale, causal, nthreads=threads())
+    return o, lse, a
+
+
+def oracle_varlen(q, k, v, cu, scale, causal):
+    o, lse = oracle.attention_varlen(q, k, v, cu, scale, causal, nthreads=threads())
+    a, _ = oracle.attention_varlen(q, k, v.abs(), cu, scale, causal, nthreads=threads())
+    return o, lse, a
