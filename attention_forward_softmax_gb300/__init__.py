@@ -40,7 +40,7 @@ class AttnError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _build
+    from ._builder import build as _build
     return _build(force=force)
 
 
