@@ -27,7 +27,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
           6: "ATTN_ERR_BAD_SEQLENS", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_TOO_LARGE"}
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_fp8", "qkv_block_quant_hadamard",
-           "attn_get_status", "attn_status_string", "attn_shutdown", "attn_version")
+           "attn_get_status", "attn_fwd_varlen_noalloc", "attn_status_string",
+           "attn_shutdown", "attn_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -59,11 +60,13 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
             L.qkv_block_quant_hadamard.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i,
                                                    i, i, i, i, vp]
+            L.attn_fwd_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i,
+                                                  i, vp, vp]
             L.attn_get_status.argtypes = [vp]
             L.attn_status_string.argtypes = [i]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_version.restype = ctypes.c_uint32
-            for nm in EXPORTS[:5]:
+            for nm in EXPORTS[:6]:
                 getattr(L, nm).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -135,6 +138,25 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
                                int(bool(causal)), _dtype_code(q), _stream(stream))
     _check(rc, "attn_fwd_varlen")
     return o, lse
+
+
+def attn_fwd_varlen_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, lse=None, status=None,
+                            causal: bool = False, scale: float | None = None, stream=None):
+    """attn_fwd_varlen for callers that cannot allocate device memory: the
+    caller supplies every buffer (`out`, optional `lse` [H,T] fp32, optional
+    one-element int32 `status` on the device) and the library uses only its
+    fixed static scratch.  This wrapper allocates nothing either."""
+    _need_cuda(q, k, v, cu_seqlens, out, lse, status)
+    T, H, d = q.shape
+    if cu_seqlens.dtype != torch.int32 or (status is not None and status.dtype != torch.int32):
+        raise TypeError("cu_seqlens and status must be int32")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib().attn_fwd_varlen_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                       _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                       int(max_seqlen), H, d, scale, int(bool(causal)),
+                                       _dtype_code(q), _ptr(status), _stream(stream))
+    _check(rc, "attn_fwd_varlen_noalloc")
+    return out, lse
 
 
 def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool = False,

@@ -48,6 +48,11 @@ struct DeviceState {
   unsigned attr_done = 0;       // bit per kernel instantiation: smem attribute set
 };
 attn_status_t device_state(DeviceState **out);
+
+// Launches the varlen tile-list builder (one CTA) on `s`.
+cudaError_t launch_varlen_schedule(const int *cu_seqlens, int nseq, int total_tokens,
+                                   int max_seqlen, int causal, int2 *tiles, int capacity,
+                                   int *num_entries, int *status, cudaStream_t s);
 attn_status_t ensure_tiles(DeviceState *ds, size_t entries);
 long long wait_budget();
 

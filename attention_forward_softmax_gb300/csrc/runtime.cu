@@ -152,6 +152,15 @@ __global__ void __launch_bounds__(kSchedThreads)
   }
 }
 
+cudaError_t launch_varlen_schedule(const int *cu_seqlens, int nseq, int total_tokens,
+                                   int max_seqlen, int causal, int2 *tiles, int capacity,
+                                   int *num_entries, int *status, cudaStream_t s) {
+  varlen_schedule_kernel<<<1, kSchedThreads, 0, s>>>(cu_seqlens, nseq, total_tokens, max_seqlen,
+                                                     causal ? 1 : 0, tiles, capacity, num_entries,
+                                                     status);
+  return cudaGetLastError();
+}
+
 namespace {
 
 attn_status_t check_common(const void *q, const void *k, const void *v, const void *o,

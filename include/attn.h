@@ -91,6 +91,39 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
                               attn_dtype_t dtype, void *stream);
 
 /*
+ * attn_fwd_varlen without any device allocation.  (The paper has no
+ * counterpart: this is a calling convention of this library, not a step of
+ * the method.)
+ *
+ * Same operation, arguments and result as attn_fwd_varlen, for callers that
+ * cannot allocate device memory -- a plugin or custom op whose device memory
+ * is planned by a host framework or inference runtime, or a service that
+ * forbids allocation after start-up.  attn_fwd_varlen calls cudaMalloc on
+ * first use and cudaFree when its tile list must grow; this call never
+ * allocates or frees.  Its scratch (status word, tile list) is one
+ * file-scope device array of 256 + 8 * 32768 bytes (about 256 KiB) that
+ * every GPU loading the library holds until the process exits.
+ *   status : DEVICE int32 (may be NULL).  Set to 0 on `stream` at the start
+ *            of the call; a device-detected error (ATTN_ERR_BAD_SEQLENS,
+ *            ATTN_ERR_TIMEOUT) is then written there.  With NULL such errors
+ *            are not reported.  attn_get_status() does not see this call.
+ * Limits: total_tokens / 256 + nseq must not exceed 32768 (the tile list's
+ * capacity); larger problems are rejected with ATTN_ERR_TOO_LARGE before any
+ * device work.
+ * Set-up: the first call on each device looks up the device address of the
+ * scratch array and the SM count, with that device current (no allocation).
+ * Make that first call before any stream capture.
+ * Sharing: every call on a device uses the same scratch, which keeps the
+ * last call's contents.  Calls that overlap on the GPU (on different streams,
+ * or from different host threads) race on it: serialise them.
+ */
+attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, const int32_t *cu_seqlens, int nseq,
+                                      int total_tokens, int max_seqlen, int H, int d,
+                                      float scale, int causal, attn_dtype_t dtype,
+                                      int32_t *status, void *stream);
+
+/*
  * 8-bit attention forward (e4m3 operands, block scales).
  *   q8, k8, v8 : [B, N, H, d] e4m3 codes (uint8 storage), as produced by
  *                qkv_block_quant_hadamard (Q and K possibly rotated: the
