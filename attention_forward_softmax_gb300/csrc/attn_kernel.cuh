@@ -461,16 +461,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           l_run *= alpha;
           m_run = m_new;
         }
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < C::D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-        }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         float rs = 0.f;
         if constexpr (!C::kFp8) {
@@ -503,6 +493,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tmem_st32(tS, pk);
         }
         l_run += rs;
+        // Rescale O after P is stored, when the score row is no longer live
+        // (O_X may change until P_X(j) is published; PV_X(j) waits for that).
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
         tc_fence_before();
         mbar_arrive(&bar_p_full[x]);
       }
