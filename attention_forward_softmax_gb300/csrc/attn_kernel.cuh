@@ -78,6 +78,7 @@ struct Cfg {
                                 ? 8
                                 : (kSmemBudget - 2 * kTileBytes) / kTileBytes;
   static_assert(NS >= 3, "K/V ring too small");
+  static_assert((NS & (NS - 1)) == 0, "K/V ring size must be a power of two");
   // MMA shapes.  Each instruction consumes 32 bytes of K per row.
   static constexpr int kKStep = 32 / kElt;             // 16 (16-bit) or 32 (e4m3)
   static constexpr int kQKSteps = kRowBytes / 32;
@@ -285,43 +286,57 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // MMA issuer
     // ------------------------------------------------------------------
     if (lane == 0) {
-      const uint32_t sQa = smem_addr(sQ);
-      const uint32_t sKVa = smem_addr(sKV);
-      int kv_pos = 0, tcount = 0;
-      int p_cnt[2] = {0, 0};
+      // Shared-memory descriptors are built once.  Per MMA only a constant
+      // (the byte offset >> 4) is added to the low word, whose start-address
+      // field [0,14) has room for any shared-memory offset, so no carry
+      // reaches the other fields: one integer add per operand per MMA.
+      const uint64_t q0 = sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t k0 = sdesc_sw128(smem_addr(sKV), 16, 1024);
+      const uint64_t v0 = sdesc_sw128(smem_addr(sKV), C::kChunkBytes, 1024);
+      const uint32_t q_lo = static_cast<uint32_t>(q0), q_hi = static_cast<uint32_t>(q0 >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(k0), k_hi = static_cast<uint32_t>(k0 >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(v0), v_hi = static_cast<uint32_t>(v0 >> 32);
+      auto desc = [](uint32_t lo, uint32_t hi) { return (static_cast<uint64_t>(hi) << 32) | lo; };
+      unsigned kv_pos = 0;
+      int tcount = 0;
+      unsigned p_cnt[2] = {0, 0};
       bool ok = true;
       TileInfo ti;
 
       // S_X = Q_X K^T  (K tile at ring position pos)
-      auto issue_qk = [&](int x, int pos) {
-        const uint32_t qa = sQa + x * C::kTileBytes;
-        const uint32_t ka = sKVa + (pos % C::NS) * C::kTileBytes;
+      auto issue_qk = [&](int x, unsigned pos) {
+        const uint32_t qa = q_lo + static_cast<uint32_t>(x * (C::kTileBytes >> 4));
+        const uint32_t ka = k_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
+        const uint32_t d = tmem + x * C::kColS;
 #pragma unroll
         for (int s = 0; s < C::kQKSteps; ++s) {
-          const uint32_t off = (s / 4) * C::kChunkBytes + (s % 4) * 32;
-          const uint64_t ad = sdesc_sw128(qa + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(ka + off, 16, 1024);
+          const uint32_t off = ((s / 4) * C::kChunkBytes + (s % 4) * 32) >> 4;
           if constexpr (C::kFp8)
-            mma_f8_ss(tmem + x * C::kColS, ad, bd, C::kIdescQK, s > 0);
+            mma_f8_ss(d, desc(qa + off, q_hi), desc(ka + off, k_hi), C::kIdescQK, s > 0);
           else
-            mma_f16_ss(tmem + x * C::kColS, ad, bd, C::kIdescQK, s > 0);
+            mma_f16_ss(d, desc(qa + off, q_hi), desc(ka + off, k_hi), C::kIdescQK, s > 0);
         }
       };
       // O_X (+)= P_X V  (V tile at ring position pos)
-      auto issue_pv = [&](int x, int pos, bool accumulate) {
-        const uint32_t va = sKVa + (pos % C::NS) * C::kTileBytes;
+      auto issue_pv = [&](int x, unsigned pos, bool accumulate) {
+        const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
+        const uint32_t d = tmem + C::kColO0 + x * C::D;
+        const uint32_t pa = tmem + x * C::kColS;
+        if constexpr (C::kFp8)
+          mma_f8_ts(d, pa, desc(va, v_hi), C::kIdescPV, accumulate);
+        else
+          mma_f16_ts(d, pa, desc(va, v_hi), C::kIdescPV, accumulate);
 #pragma unroll
-        for (int s = 0; s < C::kPVSteps; ++s) {
-          const uint64_t bd = sdesc_sw128(va + s * C::kKStep * 128, C::kChunkBytes, 1024);
-          const uint32_t pa = tmem + x * C::kColS + s * 8;
+        for (int s = 1; s < C::kPVSteps; ++s) {
+          const uint32_t off = (s * C::kKStep * 128) >> 4;
           if constexpr (C::kFp8)
-            mma_f8_ts(tmem + C::kColO0 + x * C::D, pa, bd, C::kIdescPV, (accumulate || s > 0));
+            mma_f8_ts(d, pa + s * 8, desc(va + off, v_hi), C::kIdescPV, 1);
           else
-            mma_f16_ts(tmem + C::kColO0 + x * C::D, pa, bd, C::kIdescPV, (accumulate || s > 0));
+            mma_f16_ts(d, pa + s * 8, desc(va + off, v_hi), C::kIdescPV, 1);
         }
       };
-      auto wait_kv = [&](int pos) {
-        if (!mbar_wait(&bar_kv_full[pos % C::NS], (pos / C::NS) & 1, wc)) return false;
+      auto wait_kv = [&](unsigned pos) {
+        if (!mbar_wait(&bar_kv_full[pos & (C::NS - 1)], (pos / C::NS) & 1, wc)) return false;
         tc_fence_after();
         return true;
       };
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
         tc_fence_after();
         for (int j = 0; j < nB; ++j) {
-          const int pk = kv_pos + 2 * j, pv = pk + 1;
+          const unsigned pk = kv_pos + 2 * j, pv = pk + 1;
           if (!wait_kv(pk)) { ok = false; break; }
           if (j < nA) {
             issue_qk(0, pk);
@@ -351,11 +366,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             if (j - 1 >= nA && !wait_kv(pv - 2)) { ok = false; break; }
             issue_pv(1, pv - 2, j - 1 > 0);
-            mma_commit(&bar_kv_empty[(pv - 2) % C::NS]);
+            mma_commit(&bar_kv_empty[(pv - 2) & (C::NS - 1)]);
           }
           issue_qk(1, pk);
           mma_commit(&bar_s_full[1]);
-          mma_commit(&bar_kv_empty[pk % C::NS]);
+          mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
           if (j == nB - 1) mma_commit(bar_q_empty);
           if (j < nA) {   // O_A (+)= P_A(j) V_j
             if (!wait_p(0)) { ok = false; break; }
@@ -371,7 +386,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) break;
         {   // O_B (+)= P_B(nB-1) V_{nB-1}
           const int j = nB - 1;
-          const int pv = kv_pos + 2 * j + 1;
+          const unsigned pv = kv_pos + 2 * j + 1;
           if (!wait_p(1)) { ok = false; break; }
           if (j == 0) {
             if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
@@ -380,7 +395,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (j >= nA && !wait_kv(pv)) { ok = false; break; }
           issue_pv(1, pv, j > 0);
           mma_commit(&bar_o_final[1]);
-          mma_commit(&bar_kv_empty[pv % C::NS]);
+          mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
         }
         kv_pos += 2 * nB;
       }

@@ -3,14 +3,14 @@
 // pass (FP8, Hopper)": one scale per block of Q, K and V; Q and K multiplied
 // by a random-sign diagonal times a Hadamard matrix before quantisation).
 //
-// One CTA per (tensor, batch, head, 128-token block).  Each warp owns 16
-// token rows; a row of d channels is spread over the 32 lanes (d/32
+// One CTA per (tensor, batch, head, 128-token block).  Each of its 16 warps
+// owns 8 token rows; a row of d channels is spread over the 32 lanes (d/32
 // consecutive channels per lane).  For Q and K the row is multiplied by the
 // signs, then transformed by a fast Walsh-Hadamard transform (butterflies
 // inside a lane, then across lanes with shuffles), then scaled by 1/sqrt(d);
 // this equals x * diag(s) * H_d / sqrt(d) with H_d the Sylvester matrix.
 // The block's amax is reduced through shared memory, scale = amax / 448, and
-// every value is divided by the scale and rounded to e4m3 (nearest even,
+// every value is multiplied by 1/scale and rounded to e4m3 (nearest even,
 // saturating).  HBM-bound: 2 bytes read and 1 byte written per element.
 #include <cmath>
 
@@ -21,8 +21,8 @@ namespace attn {
 
 namespace {
 
-constexpr int kQThreads = 256;
-constexpr int kRowsPerWarp = 16;
+constexpr int kQThreads = 512;
+constexpr int kRowsPerWarp = 8;
 
 struct QuantArgs {
   const __nv_bfloat16 *x[3];
@@ -51,7 +51,10 @@ __global__ void __launch_bounds__(kQThreads)
 #pragma unroll
   for (int e = 0; e < EPL; ++e) sg[e] = rotate ? static_cast<float>(a.signs[lane * EPL + e]) : 1.f;
 
-  const __nv_bfloat16 *xin = a.x[tensor];
+  // select the tensor's pointers in registers (indexing the parameter arrays
+  // with a runtime index would copy them to local memory)
+  const __nv_bfloat16 *xin = tensor == 0 ? a.x[0] : (tensor == 1 ? a.x[1] : a.x[2]);
+  float *dsc = tensor == 0 ? a.descale[0] : (tensor == 1 ? a.descale[1] : a.descale[2]);
   const int t0 = blk * 128 + warp * kRowsPerWarp;
   float v[kRowsPerWarp][EPL];
   float amax = 0.f;
@@ -123,13 +126,14 @@ __global__ void __launch_bounds__(kQThreads)
 
   const size_t dslot = (static_cast<size_t>(b) * a.H + h) * a.nblk + blk;
   if (a.mode == 1) {
-    if (threadIdx.x == 0) a.descale[tensor][dslot] = bmax;
+    if (threadIdx.x == 0) dsc[dslot] = bmax;
     return;
   }
   const float amx = (a.mode == 2) ? a.tensor_amax[tensor] : bmax;
   const float scale = amx > 0.f ? amx / 448.f : 1.f;
-  if (threadIdx.x == 0) a.descale[tensor][dslot] = scale;
-  uint8_t *yout = a.y[tensor];
+  const float inv = 1.f / scale;   // codes from x * (1/scale): within 2 ulp of x / scale
+  if (threadIdx.x == 0) dsc[dslot] = scale;
+  uint8_t *yout = tensor == 0 ? a.y[0] : (tensor == 1 ? a.y[1] : a.y[2]);
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
     const int t = t0 + r;
@@ -137,10 +141,9 @@ __global__ void __launch_bounds__(kQThreads)
     const size_t off = ((static_cast<size_t>(b) * a.N + t) * a.H + h) * D + lane * EPL;
     if constexpr (EPL == 4) {
       *reinterpret_cast<uint32_t *>(yout + off) =
-          pack_e4m3x4(__fdiv_rn(v[r][0], scale), __fdiv_rn(v[r][1], scale),
-                      __fdiv_rn(v[r][2], scale), __fdiv_rn(v[r][3], scale));
+          pack_e4m3x4(v[r][0] * inv, v[r][1] * inv, v[r][2] * inv, v[r][3] * inv);
     } else {
-      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[r][0], scale), __fdiv_rn(v[r][1], scale), 0.f, 0.f);
+      const uint32_t w = pack_e4m3x4(v[r][0] * inv, v[r][1] * inv, 0.f, 0.f);
       *reinterpret_cast<uint16_t *>(yout + off) = static_cast<uint16_t>(w & 0xFFFFu);
     }
   }
