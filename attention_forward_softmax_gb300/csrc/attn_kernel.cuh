@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl wc{abort_flag, p.status, p.wait_budget};
   const int num_tiles = tile_count<C>(p);
-
   if (warp == 9) {
     // ------------------------------------------------------------------
     // TMA producer
@@ -462,11 +461,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (kbase + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max: four independent chains of three-input maxima
+        float mq[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mq[u] = __uint_as_float(sr[u][0]);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+          for (int i = 1; i < 31; i += 2)
+            mq[c] = fmax3(mq[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mq[c] = fmaxf(mq[c], __uint_as_float(sr[c][31]));
+        const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
         const float m_tile = mx * cs;
         const float m_new = fmaxf(m_run, m_tile);
         const bool resc = m_new > m_run + C::kRescaleThresh;
@@ -479,18 +485,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         float rs = 0.f;
         if constexpr (!C::kFp8) {
+          // x = s * cs - m in packed pairs; four independent packed row sums
+          float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), cs, -m_use));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), cs, -m_use));
-              rs += p0 + p1;
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), cs,
+                    cs, -m_use, -m_use);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
               pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
             }
             tmem_st16(tS + c * 16, pk);
           }
+          rs = ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
         } else {
           uint32_t pk[32];
 #pragma unroll
