@@ -74,9 +74,11 @@ struct Cfg {
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 bytes
   static constexpr int kTileBytes = 128 * kRowBytes;   // one Q sub-tile / K or V tile
   static constexpr int kSmemBudget = 200 * 1024;
-  static constexpr int NS = (kSmemBudget - 2 * kTileBytes) / kTileBytes > 8
-                                ? 8
-                                : (kSmemBudget - 2 * kTileBytes) / kTileBytes;
+  // K/V ring: the largest power of two of tiles (at most 8) that fits beside
+  // the two Q sub-tiles and, for e4m3, the two P tiles
+  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 2 * (kFp8 ? 128 * 128 : 0)) /
+                                  kTileBytes;
+  static constexpr int NS = kRingFit >= 8 ? 8 : (kRingFit >= 4 ? 4 : 2);
   static_assert(NS >= 3, "K/V ring too small");
   static_assert((NS & (NS - 1)) == 0, "K/V ring size must be a power of two");
   // MMA shapes.  Each instruction consumes 32 bytes of K per row.
@@ -90,16 +92,23 @@ struct Cfg {
   static constexpr uint32_t kColS = 128;              // S_X starts at column x * kColS
   static constexpr uint32_t kColO0 = 256;
   static constexpr int kPCols = BN * kElt / 4;         // 64 (16-bit P) or 32 (e4m3 P)
-  // Output rescale threshold in log2 units.  16-bit P may grow to 2^8 before
-  // a rescale; e4m3 P is stored as p * (256 * dv_j / dv_max) and must stay
-  // below 448, so there the threshold is log2(1.74).
-  static constexpr float kRescaleThresh = kFp8 ? 0.8f : 8.0f;
+  // Output rescale threshold in log2 units: p may grow to 2^thresh between
+  // rescales.  16-bit P: 2^8.  e4m3 P is stored as p * (kP8Scale * dv_j /
+  // dv_max) <= 2^3.75 * 32 = 430, below the e4m3 maximum 448.
+  static constexpr float kP8Scale = 32.f;
+  static constexpr float kRescaleThresh = kFp8 ? 3.75f : 8.0f;
+  // e4m3: P goes to shared memory (one 128 x 128-byte tile per sub-tile, the
+  // 128-byte-swizzled K-major layout), so S can be overwritten as soon as the
+  // softmax has read it; 16-bit P stays in TMEM over S.
+  static constexpr bool kSmemP = kFp8;
+  static constexpr int kPTileBytes = kSmemP ? 128 * 128 : 0;
   static constexpr int kThreads = 320;
   // shared memory layout (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffKV + NS * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NS + 8 + 1;
+  static constexpr int kOffP = kOffKV + NS * kTileBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NS + 12 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
 };
@@ -192,6 +201,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *bar_o_final = bar_s_full + 4;          // [2]
   uint64_t *bar_o_free = bar_s_full + 6;           // [2]
   uint64_t *bar_drain = bar_s_full + 8;
+  uint64_t *bar_s_free = bar_s_full + 9;           // [2] e4m3: softmax has read S
+  uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3: an O update completed
+  uint8_t *sP = smem + C::kOffP;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -212,6 +224,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&bar_o_free[x], 128);
     }
     mbar_init(bar_drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s_free[x], 128);
+      mbar_init(&bar_o_done[x], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -334,6 +350,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mma_f16_ts(d, pa + s * 8, desc(va + off, v_hi), C::kIdescPV, 1);
         }
       };
+      // O_X (+)= P_X V with P_X in shared memory (e4m3 path)
+      const uint64_t p0d = sdesc_sw128(smem_addr(sP), 16, 1024);
+      const uint32_t p_lo = static_cast<uint32_t>(p0d), p_hi = static_cast<uint32_t>(p0d >> 32);
+      auto issue_pv_smem = [&](int x, unsigned pos, bool accumulate) {
+        const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
+        const uint32_t pa = p_lo + static_cast<uint32_t>(x * (C::kPTileBytes >> 4));
+        const uint32_t d = tmem + C::kColO0 + x * C::D;
+        mma_f8_ss(d, desc(pa, p_hi), desc(va, v_hi), C::kIdescPV, accumulate);
+#pragma unroll
+        for (int s = 1; s < C::kPVSteps; ++s)
+          mma_f8_ss(d, desc(pa + ((s * 32) >> 4), p_hi),
+                    desc(va + ((s * C::kKStep * 128) >> 4), v_hi), C::kIdescPV, 1);
+      };
+      unsigned qk_cnt[2] = {0, 0};
+      // e4m3: QK_X may overwrite S_X once the softmax has read the previous S_X
+      auto wait_s_free = [&](int x) {
+        if (qk_cnt[x] > 0 && !mbar_wait(&bar_s_free[x], (qk_cnt[x] - 1) & 1, wc)) return false;
+        ++qk_cnt[x];
+        tc_fence_after();
+        return true;
+      };
       auto wait_kv = [&](unsigned pos) {
         if (!mbar_wait(&bar_kv_full[pos & (C::NS - 1)], (pos / C::NS) & 1, wc)) return false;
         tc_fence_after();
@@ -346,6 +383,57 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         return true;
       };
 
+      if constexpr (C::kSmemP) {
+        // e4m3 order per key block j: S_A(j), S_B(j) (each as soon as the
+        // softmax has read its previous S), then O_A, O_B += P(j-1) V_{j-1}.
+        for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+          const int nA = ti.nA, nB = ti.nB;
+          if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          for (int j = 0; j <= nB; ++j) {
+            if (j < nB) {
+              const unsigned pk = kv_pos + 2 * j;
+              if (!wait_kv(pk)) { ok = false; break; }
+              if (j < nA) {
+                if (!wait_s_free(0)) { ok = false; break; }
+                issue_qk(0, pk);
+                mma_commit(&bar_s_full[0]);
+              }
+              if (!wait_s_free(1)) { ok = false; break; }
+              issue_qk(1, pk);
+              mma_commit(&bar_s_full[1]);
+              mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
+              if (j == nB - 1) mma_commit(bar_q_empty);
+            }
+            if (j >= 1) {
+              const int jj = j - 1;
+              const unsigned pv = kv_pos + 2 * jj + 1;
+              if (jj < nA) {
+                if (!wait_p(0)) { ok = false; break; }
+                if (jj == 0) {
+                  if (!mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+                  tc_fence_after();
+                }
+                if (!wait_kv(pv)) { ok = false; break; }
+                issue_pv_smem(0, pv, jj > 0);
+                mma_commit(&bar_o_done[0]);
+                if (jj == nA - 1) mma_commit(&bar_o_final[0]);
+              }
+              if (!wait_p(1)) { ok = false; break; }
+              if (jj == 0) {
+                if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+                tc_fence_after();
+              }
+              if (jj >= nA && !wait_kv(pv)) { ok = false; break; }
+              issue_pv_smem(1, pv, jj > 0);
+              mma_commit(&bar_o_done[1]);
+              if (jj == nB - 1) mma_commit(&bar_o_final[1]);
+              mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
+            }
+          }
+          kv_pos += 2 * nB;
+        }
+      } else
       for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
         const int nA = ti.nA, nB = ti.nB;
         if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
@@ -414,6 +502,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t tS = tmem + lane_base + x * C::kColS;
     const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
     int s_cnt = 0, tcount = 0;
+    unsigned pstore_cnt = 0;                   // e4m3: P tiles written to shared memory
+    // e4m3: this thread's row of the P tile, and its 16-byte chunk positions
+    // under the 128-byte swizzle (chunk c of row r sits at c ^ (r & 7))
+    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
     bool ok = true;
     TileInfo ti;
     for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
@@ -422,20 +514,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int row = row0 + r_in;                      // this thread's row
       float m_run = -INFINITY;                          // running max, log2 units
       float l_run = 0.f;
-      float pv_scale = 1.f;                             // e4m3: dv_max / 256
-      float dq_s = 0.f;
+      float pv_scale = 1.f;                             // e4m3: dv_max / kP8Scale
+      float dq_s = 0.f, inv_dv_max = 0.f, dk_next = 0.f, dv_next = 0.f;
       const float *dk_row = nullptr;
       const float *dv_row = nullptr;
-      float inv_dv_max = 0.f;
       if constexpr (C::kFp8) {
         const size_t base = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
         dq_s = __ldg(p.dq + base + (row0 >> 7));
         dk_row = p.dk + base;
         dv_row = p.dv + base;
         float dvm = 0.f;
-        for (int i = 0; i < (ti.L + 127) / 128; ++i) dvm = fmaxf(dvm, __ldg(dv_row + i));
-        inv_dv_max = 256.f / dvm;
-        pv_scale = dvm / 256.f;
+        for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
+        inv_dv_max = C::kP8Scale / dvm;
+        pv_scale = dvm / C::kP8Scale;
+        dk_next = __ldg(dk_row);
+        dv_next = __ldg(dv_row);
       }
       for (int j = 0; j < nX; ++j) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
@@ -444,12 +539,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-        // scale of this key block (log2 units per raw score)
+        if constexpr (C::kSmemP) {   // S is in registers: the tensor core may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bar_s_free[x]);
+        }
+        // scale of this key block (log2 units per raw score); e4m3: the
+        // block's descales, prefetched one block ahead
         float cs = p.scale_log2;
         float pw = 1.f;                                   // e4m3: P prescale
         if constexpr (C::kFp8) {
-          cs *= dq_s * __ldg(dk_row + j);
-          pw = __ldg(dv_row + j) * inv_dv_max;
+          cs *= dq_s * dk_next;
+          pw = dv_next * inv_dv_max;
+          if (j + 1 < nX) {
+            dk_next = __ldg(dk_row + j + 1);
+            dv_next = __ldg(dv_row + j + 1);
+          }
         }
         const int kbase = j * 128;
         const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
@@ -503,20 +607,46 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
           rs = ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
         } else {
+          // p = 2^(s*cs - m) in f16 pairs (the exponential unit evaluates two
+          // per instruction; the exponent is centred on the running max so
+          // its f16 rounding is finest where p is largest), row sums of p by
+          // an f16 add tree per 32 keys then in fp32, stored value p * pw
+          const uint32_t pw2 = pack_f16x2(pw, pw);
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            uint32_t e[16];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float q4[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                q4[u] = ex2(fmaf(__uint_as_float(sr[c][4 * i + u]), cs, -m_use));
-                rs += q4[u];
-              }
-              pk[c * 8 + i] = pack_e4m3x4(q4[0] * pw, q4[1] * pw, q4[2] * pw, q4[3] * pw);
+              float x0, x1, x2, x3;
+              ffma2(x0, x1, __uint_as_float(sr[c][4 * i]), __uint_as_float(sr[c][4 * i + 1]), cs, cs,
+                    -m_use, -m_use);
+              ffma2(x2, x3, __uint_as_float(sr[c][4 * i + 2]), __uint_as_float(sr[c][4 * i + 3]),
+                    cs, cs, -m_use, -m_use);
+              e[2 * i] = ex2_f16x2(pack_f16x2(x0, x1));
+              e[2 * i + 1] = ex2_f16x2(pack_f16x2(x2, x3));
+              pk[c * 8 + i] = pack_e4m3x4_h(hmul2(e[2 * i], pw2), hmul2(e[2 * i + 1], pw2));
             }
-          tmem_st32(tS, pk);
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+              for (int i = 0; i < w; ++i) e[i] = hadd2(e[i], e[i + w]);
+            rs += f16x2_hsum(e[0]);
+          }
+          // The previous O_X update must be complete before O_X is rescaled
+          // and before its P tile is overwritten.
+          if (pstore_cnt > 0 &&
+              !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          ++pstore_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(p_row + ((c ^ (r_in & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
+          fence_proxy_async_smem();
         }
         l_run += rs;
         // Rescale O after P is stored, when the score row is no longer live

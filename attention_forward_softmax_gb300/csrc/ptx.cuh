@@ -285,6 +285,53 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Two floats -> f16x2 (first argument in the low half), round to nearest.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// 2^x for both halves of an f16x2 (hardware approximation, ~1e-3 relative).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t d;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Sum of the two halves of an f16x2, in fp32.
+__device__ __forceinline__ float f16x2_hsum(uint32_t a) {
+  __half2 h = *reinterpret_cast<__half2 *>(&a);
+  return __low2float(h) + __high2float(h);
+}
+// Two f16x2 -> four e4m3 codes (nearest even, saturating); element order kept
+// (low half of `lo` in the lowest byte).
+__device__ __forceinline__ uint32_t pack_e4m3x4_h(uint32_t lo, uint32_t hi) {
+  uint16_t a, b;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(a) : "r"(lo));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(b) : "r"(hi));
+  return (uint32_t)a | ((uint32_t)b << 16);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes visible to later
+// async-proxy reads (tensor-core operand fetches) once synchronised.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

@@ -113,7 +113,8 @@ def test_fp8_b4_h16_n8192_d128():
     """fp8 e4m3 with block scales and incoherent processing: RMSE against the
     fp64 oracle on the unrotated bf16 inputs <= 1.2e-2 and below the
     per-tensor-scale baseline; lse against the oracle run on the dequantised
-    e4m3 inputs the kernel actually sees within 1e-3."""
+    e4m3 inputs the kernel actually sees within 2^-8 (the relative error of
+    the row sum, which adds f16 exponentials)."""
     w = W.FP8
     x = W.make_inputs(w)
     q, k, v = (x[n].cuda() for n in "qkv")
@@ -142,4 +143,4 @@ def test_fp8_b4_h16_n8192_d128():
     _, lse_deq = oracle.attention_rows(qd, kd, vd, w.cu_seqlens(), w.scale, False, toks, heads,
                                        threads())
     _, lg = gpu_rows(w, o, lse, toks, heads)
-    assert float(np.abs(lg - lse_deq).max()) <= 1e-3
+    assert float(np.abs(lg - lse_deq).max()) <= 2.0 ** -8

@@ -113,11 +113,17 @@ def test_fp8_attention_rmse_vs_fp64_and_baseline(causal):
 
 def test_fp8_kernel_arithmetic_on_its_own_inputs():
     """Against the oracle run on the dequantised e4m3 inputs the kernel sees
-    (the rotation cancels), the error left is the kernel's own: P stored as
-    e4m3 p*w (w = 256 dv_j / dv_max; 3 mantissa bits: relative error <= 2^-4
-    where p*w >= 2^-6, absolute <= 2^-10 / w below that) and the bf16 output
-    (<= 2^-8 |O|).  The scores themselves are exact up to fp32 accumulation,
-    so lse must match to 1e-3."""
+    (the rotation cancels), the error left is the kernel's own:
+      * P is stored as e4m3(p * w), w = 32 dv_j / dv_max: relative error
+        <= 2^-4 where p*w >= 2^-6 (3 mantissa bits), absolute <= 2^-10 / w
+        below that; the exponential itself is evaluated in f16 pairs
+        (input and result rounding, < 2^-8 relative);
+      * the row sum l adds the f16 exponentials (input and result rounding,
+        ~2^-11 each near the row max) in an f16 tree per 32 keys (at most
+        5 roundings of 2^-11) then in fp32: relative error < 2^-8; O is
+        rounded to bf16 (2^-8 relative).
+    The scores are exact up to fp32 accumulation, so lse = m + log l is off
+    by at most the relative error of l: < 2^-8."""
     B, N, H, d = 1, 700, 2, 128
     q, k, v = outlier_qkv(4300, (B, N, H, d))
     signs = random_signs(4300, d)
@@ -128,13 +134,14 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     vd = oracle.dequantize(v8.cpu().numpy(), dvn)
     o_ref, lse_ref = oracle.attention(qd, kd, vd, 1 / math.sqrt(d), False, nthreads=threads())
     a_ref, _ = oracle.attention(qd, kd, np.abs(vd), 1 / math.sqrt(d), False, nthreads=threads())
-    assert float(np.abs(lse - lse_ref).max()) <= 1e-3
-    # subnormal P: sum_k 2^-10 / w_min |v_k| / l, with l >= 2^-0.8 (the kernel's
-    # running max is at most 0.8 (log2) below the true row max)
-    w_min = 256.0 * (dvn.min(axis=2) / dvn.max(axis=2))            # [B, H]
+    print(f"fp8 kernel vs oracle on its own inputs: max |dlse| {np.abs(lse - lse_ref).max():.2e}")
+    assert float(np.abs(lse - lse_ref).max()) <= 2.0 ** -8
+    # subnormal P: sum_k 2^-10 / w_min |v_k| / l, with l >= 1 (the largest
+    # p of a row is at least 2^0)
+    w_min = 32.0 * (dvn.min(axis=2) / dvn.max(axis=2))             # [B, H]
     vsum = np.abs(vd).sum(axis=1)                                   # [B, H, d]
-    sub = (2.0 ** -10 / w_min[..., None]) * vsum * 2.0 ** 0.8       # [B, H, d]
-    tol = 2.0 ** -4 * a_ref + 2.0 ** -8 * np.abs(o_ref) + sub[:, None] + 1e-5
+    sub = (2.0 ** -10 / w_min[..., None]) * vsum                    # [B, H, d]
+    tol = (2.0 ** -4 + 2.0 ** -8) * a_ref + 2.0 ** -7 * np.abs(o_ref) + sub[:, None] + 1e-5
     err = np.abs(o - o_ref)
     assert np.all(err <= tol), float((err - tol).max())
     print(f"fp8 kernel vs oracle on its own inputs: rmse {rmse(o, o_ref):.3e}")
