@@ -129,7 +129,7 @@ __device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, 
     const int nqt = (p.N + 255) / 256;
     const int BH = p.B * p.H;
     int bh;
-    if (p.causal) {   // heaviest query tiles first
+    if (p.causal) {   // heaviest query tiles first (longest-processing-time order)
       ti.qt = nqt - 1 - t / BH;
       bh = t % BH;
     } else {          // neighbouring CTAs share one head's K/V in L2
@@ -141,8 +141,12 @@ __device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, 
     ti.L = p.N;
     ti.start = ti.b * p.N;
   } else {
-    const int2 e = p.tiles[t / p.H];
-    ti.h = t % p.H;
+    // Heads outermost (t = h * entries + e): the CTAs running at one time
+    // share one head, whose K/V over all sequences stays in L2; within a
+    // head the list is heaviest first.
+    const int ne = num_tiles / p.H;
+    const int2 e = p.tiles[t % ne];
+    ti.h = t / ne;
     ti.b = e.x;
     ti.qt = e.y;
     ti.start = p.cu_seqlens[e.x];

@@ -3,15 +3,18 @@
 // pass (FP8, Hopper)": one scale per block of Q, K and V; Q and K multiplied
 // by a random-sign diagonal times a Hadamard matrix before quantisation).
 //
-// One CTA per (tensor, batch, head, 128-token block).  Each of its 16 warps
-// owns 8 token rows; a row of d channels is spread over the 32 lanes (d/32
-// consecutive channels per lane).  For Q and K the row is multiplied by the
-// signs, then transformed by a fast Walsh-Hadamard transform (butterflies
-// inside a lane, then across lanes with shuffles), then scaled by 1/sqrt(d);
-// this equals x * diag(s) * H_d / sqrt(d) with H_d the Sylvester matrix.
-// The block's amax is reduced through shared memory, scale = amax / 448, and
-// every value is multiplied by 1/scale and rounded to e4m3 (nearest even,
-// saturating).  HBM-bound: 2 bytes read and 1 byte written per element.
+// One CTA per (tensor, batch, head, 128-token block), 16 warps.  A token row
+// of d channels is spread over 8 lanes (d/8 consecutive channels per lane,
+// loaded as 16-byte vectors), so a warp holds 4 rows at a time and each warp
+// owns 8 rows of the block.  For Q and K the row is multiplied by the signs,
+// then transformed by a fast Walsh-Hadamard transform -- butterflies inside a
+// lane for the small strides, then across the 8 lanes with shuffles (one
+// shuffle and one fused multiply-add with a +-1 sign per element and stage)
+// -- then scaled by 1/sqrt(d); this equals x * diag(s) * H_d / sqrt(d) with
+// H_d the Sylvester matrix.  The block's amax is reduced through shared
+// memory, scale = amax / 448, and every value is multiplied by 1/scale and
+// rounded to e4m3 (nearest even, saturating).  HBM-bound: 2 bytes read and 1
+// byte written per element.
 #include <cmath>
 
 #include "internal.h"
@@ -22,7 +25,9 @@ namespace attn {
 namespace {
 
 constexpr int kQThreads = 512;
-constexpr int kRowsPerWarp = 8;
+constexpr int kLanesPerRow = 8;
+constexpr int kRowsPerPass = 32 / kLanesPerRow;          // rows a warp holds at once
+constexpr int kPasses = 128 / (kQThreads / 32) / kRowsPerPass;   // 2
 
 struct QuantArgs {
   const __nv_bfloat16 *x[3];
@@ -36,46 +41,48 @@ struct QuantArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kQThreads)
+__global__ void __launch_bounds__(kQThreads, 2)
     quant_kernel(const QuantArgs a) {
-  constexpr int EPL = D / 32;   // channels per lane
+  constexpr int EPL = D / kLanesPerRow;   // channels per lane: 16 (d=128) or 8 (d=64)
   const int tensor = blockIdx.z;
   const int bh = blockIdx.y;
   const int blk = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow;     // row within a pass
+  const int gl = lane % kLanesPerRow;      // lane within the row's group
   const bool rotate = (tensor < 2) && (a.signs != nullptr);
   __shared__ float red[kQThreads / 32];
-
-  float sg[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) sg[e] = rotate ? static_cast<float>(a.signs[lane * EPL + e]) : 1.f;
 
   // select the tensor's pointers in registers (indexing the parameter arrays
   // with a runtime index would copy them to local memory)
   const __nv_bfloat16 *xin = tensor == 0 ? a.x[0] : (tensor == 1 ? a.x[1] : a.x[2]);
   float *dsc = tensor == 0 ? a.descale[0] : (tensor == 1 ? a.descale[1] : a.descale[2]);
-  const int t0 = blk * 128 + warp * kRowsPerWarp;
-  float v[kRowsPerWarp][EPL];
-  float amax = 0.f;
+  uint8_t *yout = tensor == 0 ? a.y[0] : (tensor == 1 ? a.y[1] : a.y[2]);
+
+  // sign diagonal as a bit mask (bit e: channel gl*EPL+e is negated)
+  uint32_t sgn_bits = 0;
+  if (rotate)
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int t = t0 + r;
-    if (t < a.N) {
-      const size_t off = ((static_cast<size_t>(b) * a.N + t) * a.H + h) * D + lane * EPL;
-      if constexpr (EPL == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(xin + off);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
-        v[r][0] = __low2float(p0);
-        v[r][1] = __high2float(p0);
-        v[r][2] = __low2float(p1);
-        v[r][3] = __high2float(p1);
-      } else {
-        const uint32_t raw = *reinterpret_cast<const uint32_t *>(xin + off);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&raw);
-        v[r][0] = __low2float(p0);
-        v[r][1] = __high2float(p0);
+    for (int e = 0; e < EPL; ++e) sgn_bits |= (a.signs[gl * EPL + e] < 0 ? 1u : 0u) << e;
+
+  float v[kPasses][EPL];
+  int tok[kPasses];
+#pragma unroll
+  for (int r = 0; r < kPasses; ++r) {
+    tok[r] = blk * 128 + (warp * kPasses + r) * kRowsPerPass + sub;
+    if (tok[r] < a.N) {
+      const size_t off = ((static_cast<size_t>(b) * a.N + tok[r]) * a.H + h) * D + gl * EPL;
+#pragma unroll
+      for (int q = 0; q < EPL / 8; ++q) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(xin + off + q * 8);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[u]);
+          v[r][q * 8 + 2 * u] = __low2float(p2);
+          v[r][q * 8 + 2 * u + 1] = __high2float(p2);
+        }
       }
     } else {
 #pragma unroll
@@ -85,10 +92,11 @@ __global__ void __launch_bounds__(kQThreads)
   if (rotate) {
     const float norm = 1.f / sqrtf(static_cast<float>(D));
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
+    for (int r = 0; r < kPasses; ++r) {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[r][e] *= sg[e];
-      // butterflies between channels of one lane (strides 1, 2, ...)
+      for (int e = 0; e < EPL; ++e)
+        v[r][e] = __uint_as_float(__float_as_uint(v[r][e]) ^ (((sgn_bits >> e) & 1u) << 31));
+      // butterflies between channels of one lane (strides 1, 2, 4, ...)
 #pragma unroll
       for (int hs = 1; hs < EPL; hs <<= 1)
 #pragma unroll
@@ -98,22 +106,24 @@ __global__ void __launch_bounds__(kQThreads)
             v[r][e] = u + w;
             v[r][e + hs] = u - w;
           }
-      // butterflies across lanes (channel stride EPL * m)
+      // butterflies across the row's lanes (channel stride EPL * m): the lane
+      // holding the upper channel keeps other - mine, the lower mine + other
 #pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+      for (int m = 1; m < kLanesPerRow; m <<= 1) {
+        const float sgn = (gl & m) ? -1.f : 1.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
           const float other = __shfl_xor_sync(0xffffffffu, v[r][e], m);
-          v[r][e] = upper ? (other - v[r][e]) : (v[r][e] + other);
+          v[r][e] = fmaf(v[r][e], sgn, other);
         }
       }
 #pragma unroll
       for (int e = 0; e < EPL; ++e) v[r][e] *= norm;
     }
   }
+  float amax = 0.f;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r)
+  for (int r = 0; r < kPasses; ++r)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
 #pragma unroll
@@ -133,19 +143,19 @@ __global__ void __launch_bounds__(kQThreads)
   const float scale = amx > 0.f ? amx / 448.f : 1.f;
   const float inv = 1.f / scale;   // codes from x * (1/scale): within 2 ulp of x / scale
   if (threadIdx.x == 0) dsc[dslot] = scale;
-  uint8_t *yout = tensor == 0 ? a.y[0] : (tensor == 1 ? a.y[1] : a.y[2]);
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int t = t0 + r;
-    if (t >= a.N) break;
-    const size_t off = ((static_cast<size_t>(b) * a.N + t) * a.H + h) * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      *reinterpret_cast<uint32_t *>(yout + off) =
-          pack_e4m3x4(v[r][0] * inv, v[r][1] * inv, v[r][2] * inv, v[r][3] * inv);
-    } else {
-      const uint32_t w = pack_e4m3x4(v[r][0] * inv, v[r][1] * inv, 0.f, 0.f);
-      *reinterpret_cast<uint16_t *>(yout + off) = static_cast<uint16_t>(w & 0xFFFFu);
-    }
+  for (int r = 0; r < kPasses; ++r) {
+    if (tok[r] >= a.N) continue;
+    const size_t off = ((static_cast<size_t>(b) * a.N + tok[r]) * a.H + h) * D + gl * EPL;
+    uint32_t w[EPL / 4];
+#pragma unroll
+    for (int q = 0; q < EPL / 4; ++q)
+      w[q] = pack_e4m3x4(v[r][4 * q] * inv, v[r][4 * q + 1] * inv, v[r][4 * q + 2] * inv,
+                         v[r][4 * q + 3] * inv);
+    if constexpr (EPL == 16)
+      *reinterpret_cast<uint4 *>(yout + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint2 *>(yout + off) = make_uint2(w[0], w[1]);
   }
 }
 
