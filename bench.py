@@ -58,6 +58,23 @@ def get_workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
+def max_over_ranks(seconds: float, world: int, device) -> float:
+    """The slowest rank's time: the job finishes when every replica has."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every rank runs the full workload (replicas), so
+    the job processes world * steps steps in the slowest rank's time."""
+    return world * flops_per_rank_step * steps / seconds / 1e12
+
+
 def rank_info():
     r = int(os.environ.get("RANK", "0"))
     w = int(os.environ.get("WORLD_SIZE", "1"))
@@ -259,10 +276,7 @@ def run_gpu(args):
         t = time_region(step, args.steps, stream)
     barrier()
     agb.check_status()
-    if world > 1:
-        tt = torch.tensor([t], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(t, world, dev)
 
     # roofline leg: dominant kernel timed per launch on its own stream
     peaks, peak_kind = load_peaks()
@@ -305,15 +319,12 @@ def run_gpu(args):
     barrier()
     te = time_region(e2e, max(5, args.steps // 10), stream)
     barrier()
-    if world > 1:
-        tt = torch.tensor([te], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
+    te = max_over_ranks(te, world, dev)
     e2e_steps = max(5, args.steps // 10)
 
     result = None
     if rank == 0:
-        value = world * flops * args.steps / t / 1e12
+        value = job_tflops(world, flops, args.steps, t)
         cpu = None if args.no_cpu_baseline else cpu_baseline(w, budget_s=args.cpu_seconds)
         result = {
             "metric": "attn fwd TFLOP/s (4*B*H*N^2*d, /2 causal)",
@@ -333,7 +344,7 @@ def run_gpu(args):
             "pct_of_dense_peak": round(100 * value / world / NOMINAL_DENSE_TFLOPS[dtype], 2),
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": round(world * flops * e2e_steps / te / 1e12, 2), "unit": "TFLOP/s",
+            "e2e": {"value": round(job_tflops(world, flops, e2e_steps, te), 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(te / e2e_steps * 1e3, 4)},
             "gpu_launches": launches * args.steps,
