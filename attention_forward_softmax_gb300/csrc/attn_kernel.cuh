@@ -11,20 +11,26 @@
 // How it is laid out on the GPU (our design, not the card's Hopper one):
 //  * one CTA per SM, persistent over work tiles; a work tile is 256 query
 //    rows of one (sequence, head), split into two 128-row sub-tiles A and B;
-//  * warp roles (320 threads):
+//  * warp roles (320 threads; 352 for e4m3):
 //      warps 0-3  softmax warpgroup for sub-tile A (one thread per row)
 //      warps 4-7  softmax warpgroup for sub-tile B
 //      warp  8    MMA issuer (one thread) + TMEM allocation
 //      warp  9    TMA producer (one thread)
+//      warp 10    e4m3 only: second MMA issuer, for the O updates
 //  * Q sub-tiles stay in shared memory for the whole tile; K and V tiles of
 //    128 keys stream through a ring of NS slots (K_0, V_0, K_1, V_1, ...);
 //  * TMEM (512 columns): S_A [0,128), S_B [128,256), O_A, O_B after them;
-//    P (16-bit or e4m3) is written back over the first columns of its S;
-//  * tensor-core order per key block j:  S_A(j), O_B += P_B(j-1) V_{j-1},
-//    S_B(j), O_A += P_A(j) V_j -- so each softmax warpgroup works while the
-//    tensor core serves the other sub-tile.  A commit after S_X(j) also
-//    covers the earlier O_X update, so when softmax X sees S_X(j) ready its O
-//    is current and it may rescale O in place;
+//    16-bit P is written back over the first columns of its S; e4m3 P goes
+//    to one shared-memory tile per sub-tile;
+//  * 16-bit tensor-core order per key block j:  S_A(j), O_B += P_B(j-1)
+//    V_{j-1}, S_B(j), O_A += P_A(j) V_j -- so each softmax warpgroup works
+//    while the tensor core serves the other sub-tile.  A commit after S_X(j)
+//    also covers the earlier O_X update, so when softmax X sees S_X(j) ready
+//    its O is current and it may rescale O in place;
+//  * e4m3: S_X(j+1) is issued as soon as softmax X has read S_X(j) into
+//    registers, by its own issuing thread; O_X += P_X(j) V_j waits for the P
+//    tile, and the softmax waits for that update before it rescales O_X or
+//    rewrites the tile;
 //  * the output is rescaled only when a row max grows by more than
 //    kRescaleThresh (log2 units); otherwise the stale max is kept, which is
 //    exact after the final division by l;
@@ -73,10 +79,10 @@ struct Cfg {
   static constexpr int kChunkElems = 128 / kElt;
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 bytes
   static constexpr int kTileBytes = 128 * kRowBytes;   // one Q sub-tile / K or V tile
-  static constexpr int kSmemBudget = 200 * 1024;
+  static constexpr int kSmemBudget = 224 * 1024;
   // K/V ring: the largest power of two of tiles (at most 8) that fits beside
-  // the two Q sub-tiles and, for e4m3, the two P tiles
-  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 2 * (kFp8 ? 128 * 128 : 0)) /
+  // the two Q sub-tiles and, for e4m3, the four P tiles
+  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 4 * (kFp8 ? 128 * 128 : 0)) /
                                   kTileBytes;
   static constexpr int NS = kRingFit >= 8 ? 8 : (kRingFit >= 4 ? 4 : 2);
   static_assert(NS >= 3, "K/V ring too small");
@@ -97,18 +103,20 @@ struct Cfg {
   // dv_max) <= 2^3.75 * 32 = 430, below the e4m3 maximum 448.
   static constexpr float kP8Scale = 32.f;
   static constexpr float kRescaleThresh = kFp8 ? 3.75f : 8.0f;
-  // e4m3: P goes to shared memory (one 128 x 128-byte tile per sub-tile, the
-  // 128-byte-swizzled K-major layout), so S can be overwritten as soon as the
-  // softmax has read it; 16-bit P stays in TMEM over S.
+  // e4m3: P goes to shared memory (two 128 x 128-byte tiles per sub-tile,
+  // used in turn, in the 128-byte-swizzled K-major layout), so S can be
+  // overwritten as soon as the softmax has read it, and P_X(j) can be written
+  // while O_X += P_X(j-1) V_{j-1} still runs; 16-bit P stays in TMEM over S.
   static constexpr bool kSmemP = kFp8;
   static constexpr int kPTileBytes = kSmemP ? 128 * 128 : 0;
-  static constexpr int kThreads = 320;
+  // e4m3: a second issuing warp (warp 10) takes the O updates
+  static constexpr int kThreads = kSmemP ? 352 : 320;
   // shared memory layout (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffP = kOffKV + NS * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NS + 12 + 1;
+  static constexpr int kOffBar = kOffP + 4 * kPTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NS + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
 };
@@ -201,12 +209,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *bar_kv_full = bars + 2;
   uint64_t *bar_kv_empty = bars + 2 + C::NS;
   uint64_t *bar_s_full = bars + 2 + 2 * C::NS;     // [2]
-  uint64_t *bar_p_full = bar_s_full + 2;           // [2]
+  uint64_t *bar_p_full = bar_s_full + 2;           // [2] (e4m3: P buffer 0)
   uint64_t *bar_o_final = bar_s_full + 4;          // [2]
   uint64_t *bar_o_free = bar_s_full + 6;           // [2]
   uint64_t *bar_drain = bar_s_full + 8;
   uint64_t *bar_s_free = bar_s_full + 9;           // [2] e4m3: softmax has read S
-  uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3: an O update completed
+  uint64_t *bar_o_done = bar_s_full + 11;          // [2][2] e4m3: the O update reading
+                                                   // P buffer [x][b] completed
+  uint64_t *bar_p_full1 = bar_s_full + 15;         // [2] e4m3: P buffer 1 written
   uint8_t *sP = smem + C::kOffP;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -227,10 +237,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&bar_o_final[x], 1);
       mbar_init(&bar_o_free[x], 128);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, C::kSmemP ? 2 : 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_free[x], 128);
-      mbar_init(&bar_o_done[x], 1);
+      mbar_init(&bar_o_done[2 * x], 1);
+      mbar_init(&bar_o_done[2 * x + 1], 1);
+      mbar_init(&bar_p_full1[x], 128);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -300,9 +312,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (q_issued > 0) mbar_wait_drain(bar_q_full, (q_issued - 1) & 1);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 8 || (C::kSmemP && warp == 10)) {
     // ------------------------------------------------------------------
-    // MMA issuer
+    // MMA issuer(s)
     // ------------------------------------------------------------------
     if (lane == 0) {
       // Shared-memory descriptors are built once.  Per MMA only a constant
@@ -357,9 +369,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // O_X (+)= P_X V with P_X in shared memory (e4m3 path)
       const uint64_t p0d = sdesc_sw128(smem_addr(sP), 16, 1024);
       const uint32_t p_lo = static_cast<uint32_t>(p0d), p_hi = static_cast<uint32_t>(p0d >> 32);
+      unsigned pv_cnt[2] = {0, 0};   // e4m3: O_X updates issued (P buffer = count & 1)
       auto issue_pv_smem = [&](int x, unsigned pos, bool accumulate) {
         const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
-        const uint32_t pa = p_lo + static_cast<uint32_t>(x * (C::kPTileBytes >> 4));
+        const uint32_t pa =
+            p_lo + static_cast<uint32_t>((2 * x + (pv_cnt[x] & 1)) * (C::kPTileBytes >> 4));
         const uint32_t d = tmem + C::kColO0 + x * C::D;
         mma_f8_ss(d, desc(pa, p_hi), desc(va, v_hi), C::kIdescPV, accumulate);
 #pragma unroll
@@ -380,22 +394,33 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after();
         return true;
       };
+      // e4m3: P tile n of sub-tile X sits in buffer n & 1, each buffer with
+      // its own barrier, so a softmax one tile ahead never completes a
+      // phase this thread has not yet waited for.
       auto wait_p = [&](int x) {
-        if (!mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
+        const bool ok_p =
+            C::kSmemP ? mbar_wait((p_cnt[x] & 1) ? &bar_p_full1[x] : &bar_p_full[x],
+                                  (p_cnt[x] >> 1) & 1, wc)
+                      : mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc);
+        if (!ok_p) return false;
         ++p_cnt[x];
         tc_fence_after();
         return true;
       };
 
       if constexpr (C::kSmemP) {
-        // e4m3 order per key block j: S_A(j), S_B(j) (each as soon as the
-        // softmax has read its previous S), then O_A, O_B += P(j-1) V_{j-1}.
+        // e4m3: two issuing threads.  Warp 8 issues S_X(j) = Q_X K_j^T as
+        // soon as softmax X has read S_X(j-1); warp 10 issues
+        // O_X += P_X(j) V_j as soon as P_X(j) is in shared memory.  Each
+        // commit covers only the committing thread's MMAs, so the barrier
+        // traffic of one issuer overlaps the other's tensor work.
+        const bool qk_role = warp == 8;
         for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
           const int nA = ti.nA, nB = ti.nB;
-          if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          for (int j = 0; j <= nB; ++j) {
-            if (j < nB) {
+          if (qk_role) {
+            if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            for (int j = 0; j < nB; ++j) {
               const unsigned pk = kv_pos + 2 * j;
               if (!wait_kv(pk)) { ok = false; break; }
               if (j < nA) {
@@ -409,29 +434,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
               if (j == nB - 1) mma_commit(bar_q_empty);
             }
-            if (j >= 1) {
-              const int jj = j - 1;
-              const unsigned pv = kv_pos + 2 * jj + 1;
-              if (jj < nA) {
+          } else {
+            for (int j = 0; j < nB; ++j) {
+              const unsigned pv = kv_pos + 2 * j + 1;
+              if (j < nA) {
                 if (!wait_p(0)) { ok = false; break; }
-                if (jj == 0) {
+                if (j == 0) {
                   if (!mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
                   tc_fence_after();
                 }
                 if (!wait_kv(pv)) { ok = false; break; }
-                issue_pv_smem(0, pv, jj > 0);
-                mma_commit(&bar_o_done[0]);
-                if (jj == nA - 1) mma_commit(&bar_o_final[0]);
+                issue_pv_smem(0, pv, j > 0);
+                mma_commit(&bar_o_done[pv_cnt[0]++ & 1]);
+                if (j == nA - 1) mma_commit(&bar_o_final[0]);
               }
               if (!wait_p(1)) { ok = false; break; }
-              if (jj == 0) {
+              if (j == 0) {
                 if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
                 tc_fence_after();
               }
-              if (jj >= nA && !wait_kv(pv)) { ok = false; break; }
-              issue_pv_smem(1, pv, jj > 0);
-              mma_commit(&bar_o_done[1]);
-              if (jj == nB - 1) mma_commit(&bar_o_final[1]);
+              if (j >= nA && !wait_kv(pv)) { ok = false; break; }
+              issue_pv_smem(1, pv, j > 0);
+              mma_commit(&bar_o_done[2 + (pv_cnt[1]++ & 1)]);
+              if (j == nB - 1) mma_commit(&bar_o_final[1]);
               mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
             }
           }
@@ -507,11 +532,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
     int s_cnt = 0, tcount = 0;
     unsigned pstore_cnt = 0;                   // e4m3: P tiles written to shared memory
-    // e4m3: this thread's row of the P tile, and its 16-byte chunk positions
+    // e4m3: this thread's row of P buffer 0, and its 16-byte chunk positions
     // under the 128-byte swizzle (chunk c of row r sits at c ^ (r & 7))
-    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
+    const uint32_t p_row = smem_addr(sP) + 2 * x * C::kPTileBytes + r_in * 128;
     bool ok = true;
     TileInfo ti;
+    // e4m3: warps wq (sub-tile A) and wq + 4 (sub-tile B) share one SM
+    // sub-partition and take turns at the exponential-heavy part of a key
+    // block (named barriers turn_a / turn_b, 64 threads), so one warp's
+    // loads, stores and waits overlap the other's arithmetic.  A goes first;
+    // each tile couples the first nA key blocks of both sub-tiles.
+    const uint32_t turn_a = 1 + wq, turn_b = 5 + wq;
+    if (C::kFp8 && x == 1) named_bar_arrive(turn_a, 64);
     for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
       const int nX = x == 0 ? ti.nA : ti.nB;
       const int row0 = ti.qt * 256 + x * 128;          // first row of the sub-tile
@@ -569,6 +601,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (kbase + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
         }
+        // A turn is taken only while no wait has given up: after an abort a
+        // partner hands over at most one more turn (below the tile loop), so
+        // each warp blocks on its turn barrier at most once more.
+        const bool turn = C::kFp8 && j < ti.nA;
+        if (turn) {
+          if (*abort_flag) { ok = false; break; }
+          named_bar_sync(x == 0 ? turn_a : turn_b, 64);
+        }
         // row max: four independent chains of three-input maxima
         float mq[4];
 #pragma unroll
@@ -592,6 +632,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         float rs = 0.f;
+        uint32_t pbuf = 0;                                // e4m3: P buffer written
         if constexpr (!C::kFp8) {
           // x = s * cs - m in packed pairs; four independent packed row sums
           float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -611,46 +652,57 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
           rs = ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
         } else {
-          // p = 2^(s*cs - m) in f16 pairs (the exponential unit evaluates two
-          // per instruction; the exponent is centred on the running max so
-          // its f16 rounding is finest where p is largest), row sums of p by
-          // an f16 add tree per 32 keys then in fp32, stored value p * pw
-          const uint32_t pw2 = pack_f16x2(pw, pw);
+          // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
+          // into the exponent; row sums of the stored values in four packed
+          // fp32 accumulators, divided by pw once per key block
+          const float lpw = __log2f(fmaxf(pw, 1e-30f));
+          const float mb = m_use - lpw;
+          float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t e[16];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               float x0, x1, x2, x3;
               ffma2(x0, x1, __uint_as_float(sr[c][4 * i]), __uint_as_float(sr[c][4 * i + 1]), cs, cs,
-                    -m_use, -m_use);
+                    -mb, -mb);
               ffma2(x2, x3, __uint_as_float(sr[c][4 * i + 2]), __uint_as_float(sr[c][4 * i + 3]),
-                    cs, cs, -m_use, -m_use);
-              e[2 * i] = ex2_f16x2(pack_f16x2(x0, x1));
-              e[2 * i + 1] = ex2_f16x2(pack_f16x2(x2, x3));
-              pk[c * 8 + i] = pack_e4m3x4_h(hmul2(e[2 * i], pw2), hmul2(e[2 * i + 1], pw2));
+                    cs, cs, -mb, -mb);
+              const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+              fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
+              fadd2(ra[(i + 2) & 3], rb[(i + 2) & 3], ra[(i + 2) & 3], rb[(i + 2) & 3], p2, p3);
+              pk[c * 8 + i] = pack_e4m3x4(p0, p1, p2, p3);
             }
-#pragma unroll
-            for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-              for (int i = 0; i < w; ++i) e[i] = hadd2(e[i], e[i + w]);
-            rs += f16x2_hsum(e[0]);
           }
-          // The previous O_X update must be complete before O_X is rescaled
-          // and before its P tile is overwritten.
-          if (pstore_cnt > 0 &&
-              !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc))) {
+          rs = (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
+               ex2(-lpw);
+          if (turn) named_bar_arrive(x == 0 ? turn_b : turn_a, 64);
+          // P buffer b = g & 1 (g: P tiles written so far) is free once the
+          // O update that read it two tiles ago has completed; that update
+          // is completion (g >> 1) - 1 of the buffer's barrier.
+          const unsigned g = pstore_cnt++;
+          const uint32_t b = g & 1;
+          pbuf = b;
+          if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[2 * x + b],
+                                                           ((g >> 1) - 1) & 1, wc))) {
             ok = false;
             break;
           }
-          ++pstore_cnt;
           tc_fence_after();
+          const uint32_t prow = p_row + b * C::kPTileBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_shared_v4(p_row + ((c ^ (r_in & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+            st_shared_v4(prow + ((c ^ (r_in & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
                          pk[4 * c + 3]);
           fence_proxy_async_smem();
+          // O_X is rescaled below only after the previous update (tile g - 1,
+          // completion (g - 1) >> 1 of its buffer's barrier) has landed.
+          if (j > 0 && __any_sync(0xffffffffu, resc) &&
+              !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[2 * x + (b ^ 1)],
+                                                 ((g - 1) >> 1) & 1, wc))) {
+            ok = false;
+            break;
+          }
         }
         l_run += rs;
         // Rescale O after P is stored, when the score row is no longer live
@@ -666,7 +718,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bar_p_full[x]);
+        mbar_arrive(pbuf ? &bar_p_full1[x] : &bar_p_full[x]);
       }
       if (!ok) break;
       // ---------------- epilogue: O / l, lse ----------------
@@ -710,6 +762,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar_o_free[x]);
     }
+    // A warp that gave up (a wait ran out) hands its partner one more turn,
+    // so a partner blocked on its turn barrier is released; every other wait
+    // of the partner then sees the abort flag.  Arrivals nobody waits for
+    // are left behind at exit.
+    if (C::kFp8 && !ok) named_bar_arrive(x == 0 ? turn_b : turn_a, 64);
   }
 
   tc_fence_before();

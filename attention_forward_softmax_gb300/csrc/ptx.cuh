@@ -328,6 +328,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 // Makes this thread's generic-proxy shared-memory writes visible to later
 // async-proxy reads (tensor-core operand fetches) once synchronised.
+// Named barriers (IDs 1..15; 0 is __syncthreads).  `count` threads take
+// part, a multiple of 32; bar.arrive does not wait.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -130,6 +130,9 @@ attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, const void *
  *                rotation cancels in Q K^T).
  *   descale_q/k/v : float32 [B, H, ceil(N/128)]; block j of (b, h) covers
  *                tokens 128j .. 128j+127 and dequantises as code * descale.
+ *                Every descale must be finite and positive (the quantiser
+ *                below writes 1 for an all-zero block); other values give
+ *                undefined output.
  *   o   : [B, N, H, d] bf16;  lse : [B, H, N] float32 (may be NULL).
  * V is consumed in its stored [token, d] layout (no transpose in memory).
  */
