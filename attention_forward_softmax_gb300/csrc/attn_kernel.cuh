@@ -81,8 +81,8 @@ struct Cfg {
   static constexpr int kTileBytes = 128 * kRowBytes;   // one Q sub-tile / K or V tile
   static constexpr int kSmemBudget = 224 * 1024;
   // K/V ring: the largest power of two of tiles (at most 8) that fits beside
-  // the two Q sub-tiles and, for e4m3, the four P tiles
-  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 4 * (kFp8 ? 128 * 128 : 0)) /
+  // the two Q sub-tiles and, for e4m3, the two P tiles
+  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 2 * (kFp8 ? 128 * 128 : 0)) /
                                   kTileBytes;
   static constexpr int NS = kRingFit >= 8 ? 8 : (kRingFit >= 4 ? 4 : 2);
   static_assert(NS >= 3, "K/V ring too small");
@@ -103,22 +103,33 @@ struct Cfg {
   // dv_max) <= 2^3.75 * 32 = 430, below the e4m3 maximum 448.
   static constexpr float kP8Scale = 32.f;
   static constexpr float kRescaleThresh = kFp8 ? 3.75f : 8.0f;
-  // e4m3: P goes to shared memory (two 128 x 128-byte tiles per sub-tile,
-  // used in turn, in the 128-byte-swizzled K-major layout), so S can be
-  // overwritten as soon as the softmax has read it, and P_X(j) can be written
-  // while O_X += P_X(j-1) V_{j-1} still runs; 16-bit P stays in TMEM over S.
+  // e4m3: P goes to shared memory (one 128 x 128-byte tile per sub-tile, the
+  // 128-byte-swizzled K-major layout), so S can be overwritten as soon as the
+  // softmax has read it; 16-bit P stays in TMEM over S.
   static constexpr bool kSmemP = kFp8;
   static constexpr int kPTileBytes = kSmemP ? 128 * 128 : 0;
-  // e4m3: a second issuing warp (warp 10) takes the O updates
-  static constexpr int kThreads = kSmemP ? 352 : 320;
+  // e4m3: two softmax threads per query row (16 softmax warps)
+  static constexpr bool kSplit = kFp8;
+  static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
+  static constexpr int kWarpMMA = kSoftmaxWarps;       // MMA issuer (S = Q K^T) + TMEM allocation
+  static constexpr int kWarpTMA = kSoftmaxWarps + 1;   // TMA producer
+  static constexpr int kWarpPV = kSoftmaxWarps + 2;    // e4m3: second issuer (O += P V)
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2 + (kSmemP ? 1 : 0));
+  // arrivals per phase on the barriers the softmax signals: one per thread
+  // (16-bit), one per warp (e4m3)
+  static constexpr int kSoftArrive = kSplit ? 8 : 128;
   // shared memory layout (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffP = kOffKV + NS * kTileBytes;
-  static constexpr int kOffBar = kOffP + 4 * kPTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NS + 17;
+  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NS + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
+  // e4m3: row maxima [2][2][2][128] and row sums [2][2][128] exchanged by
+  // the two threads of a row
+  static constexpr int kOffRed = (kOffMisc + 64 + 15) / 16 * 16;
+  static constexpr int kRedBytes = kSplit ? (1024 + 512) * 4 : 0;
+  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024 /* alignment slack */ + 1024 /* guard */;
 };
 
 struct TileInfo {
@@ -209,14 +220,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *bar_kv_full = bars + 2;
   uint64_t *bar_kv_empty = bars + 2 + C::NS;
   uint64_t *bar_s_full = bars + 2 + 2 * C::NS;     // [2]
-  uint64_t *bar_p_full = bar_s_full + 2;           // [2] (e4m3: P buffer 0)
+  uint64_t *bar_p_full = bar_s_full + 2;           // [2]
   uint64_t *bar_o_final = bar_s_full + 4;          // [2]
   uint64_t *bar_o_free = bar_s_full + 6;           // [2]
   uint64_t *bar_drain = bar_s_full + 8;
   uint64_t *bar_s_free = bar_s_full + 9;           // [2] e4m3: softmax has read S
-  uint64_t *bar_o_done = bar_s_full + 11;          // [2][2] e4m3: the O update reading
-                                                   // P buffer [x][b] completed
-  uint64_t *bar_p_full1 = bar_s_full + 15;         // [2] e4m3: P buffer 1 written
+  uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3: an O update completed
   uint8_t *sP = smem + C::kOffP;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -233,25 +242,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_full[x], 1);
-      mbar_init(&bar_p_full[x], 128);
+      mbar_init(&bar_p_full[x], C::kSoftArrive);
       mbar_init(&bar_o_final[x], 1);
-      mbar_init(&bar_o_free[x], 128);
+      mbar_init(&bar_o_free[x], C::kSoftArrive);
     }
     mbar_init(bar_drain, C::kSmemP ? 2 : 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar_s_free[x], 128);
-      mbar_init(&bar_o_done[2 * x], 1);
-      mbar_init(&bar_o_done[2 * x + 1], 1);
-      mbar_init(&bar_p_full1[x], 128);
+      mbar_init(&bar_s_free[x], C::kSoftArrive);
+      mbar_init(&bar_o_done[x], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == C::kWarpMMA) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
-  if (warp == 9 && lane == 0) {
+  if (warp == C::kWarpTMA && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl wc{abort_flag, p.status, p.wait_budget};
   const int num_tiles = tile_count<C>(p);
-  if (warp == 9) {
+  if (warp == C::kWarpTMA) {
     // ------------------------------------------------------------------
     // TMA producer
     // ------------------------------------------------------------------
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (q_issued > 0) mbar_wait_drain(bar_q_full, (q_issued - 1) & 1);
       }
     }
-  } else if (warp == 8 || (C::kSmemP && warp == 10)) {
+  } else if (warp == C::kWarpMMA || (C::kSmemP && warp == C::kWarpPV)) {
     // ------------------------------------------------------------------
     // MMA issuer(s)
     // ------------------------------------------------------------------
@@ -369,11 +376,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // O_X (+)= P_X V with P_X in shared memory (e4m3 path)
       const uint64_t p0d = sdesc_sw128(smem_addr(sP), 16, 1024);
       const uint32_t p_lo = static_cast<uint32_t>(p0d), p_hi = static_cast<uint32_t>(p0d >> 32);
-      unsigned pv_cnt[2] = {0, 0};   // e4m3: O_X updates issued (P buffer = count & 1)
       auto issue_pv_smem = [&](int x, unsigned pos, bool accumulate) {
         const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
-        const uint32_t pa =
-            p_lo + static_cast<uint32_t>((2 * x + (pv_cnt[x] & 1)) * (C::kPTileBytes >> 4));
+        const uint32_t pa = p_lo + static_cast<uint32_t>(x * (C::kPTileBytes >> 4));
         const uint32_t d = tmem + C::kColO0 + x * C::D;
         mma_f8_ss(d, desc(pa, p_hi), desc(va, v_hi), C::kIdescPV, accumulate);
 #pragma unroll
@@ -394,15 +399,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after();
         return true;
       };
-      // e4m3: P tile n of sub-tile X sits in buffer n & 1, each buffer with
-      // its own barrier, so a softmax one tile ahead never completes a
-      // phase this thread has not yet waited for.
       auto wait_p = [&](int x) {
-        const bool ok_p =
-            C::kSmemP ? mbar_wait((p_cnt[x] & 1) ? &bar_p_full1[x] : &bar_p_full[x],
-                                  (p_cnt[x] >> 1) & 1, wc)
-                      : mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc);
-        if (!ok_p) return false;
+        if (!mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
         ++p_cnt[x];
         tc_fence_after();
         return true;
@@ -414,7 +412,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // O_X += P_X(j) V_j as soon as P_X(j) is in shared memory.  Each
         // commit covers only the committing thread's MMAs, so the barrier
         // traffic of one issuer overlaps the other's tensor work.
-        const bool qk_role = warp == 8;
+        const bool qk_role = warp == C::kWarpMMA;
         for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
           const int nA = ti.nA, nB = ti.nB;
           if (qk_role) {
@@ -445,7 +443,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 if (!wait_kv(pv)) { ok = false; break; }
                 issue_pv_smem(0, pv, j > 0);
-                mma_commit(&bar_o_done[pv_cnt[0]++ & 1]);
+                mma_commit(&bar_o_done[0]);
                 if (j == nA - 1) mma_commit(&bar_o_final[0]);
               }
               if (!wait_p(1)) { ok = false; break; }
@@ -455,7 +453,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               }
               if (j >= nA && !wait_kv(pv)) { ok = false; break; }
               issue_pv_smem(1, pv, j > 0);
-              mma_commit(&bar_o_done[2 + (pv_cnt[1]++ & 1)]);
+              mma_commit(&bar_o_done[1]);
               if (j == nB - 1) mma_commit(&bar_o_final[1]);
               mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
             }
@@ -520,9 +518,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_wait_drain(bar_drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if constexpr (!C::kSplit) {
     // ------------------------------------------------------------------
-    // Softmax warpgroups: x = 0 (sub-tile A) or 1 (sub-tile B)
+    // 16-bit softmax warpgroups: x = 0 (sub-tile A) or 1 (sub-tile B), one
+    // thread per query row
     // ------------------------------------------------------------------
     const int x = warp >> 2;
     const int wq = warp & 3;                 // TMEM lane quarter of this warp
@@ -531,43 +530,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t tS = tmem + lane_base + x * C::kColS;
     const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
     int s_cnt = 0, tcount = 0;
-    unsigned pstore_cnt = 0;                   // e4m3: P tiles written to shared memory
-    // e4m3: this thread's row of P buffer 0, and its 16-byte chunk positions
-    // under the 128-byte swizzle (chunk c of row r sits at c ^ (r & 7))
-    const uint32_t p_row = smem_addr(sP) + 2 * x * C::kPTileBytes + r_in * 128;
     bool ok = true;
     TileInfo ti;
-    // e4m3: warps wq (sub-tile A) and wq + 4 (sub-tile B) share one SM
-    // sub-partition and take turns at the exponential-heavy part of a key
-    // block (named barriers turn_a / turn_b, 64 threads), so one warp's
-    // loads, stores and waits overlap the other's arithmetic.  A goes first;
-    // each tile couples the first nA key blocks of both sub-tiles.
-    const uint32_t turn_a = 1 + wq, turn_b = 5 + wq;
-    if (C::kFp8 && x == 1) named_bar_arrive(turn_a, 64);
     for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
       const int nX = x == 0 ? ti.nA : ti.nB;
       const int row0 = ti.qt * 256 + x * 128;          // first row of the sub-tile
       const int row = row0 + r_in;                      // this thread's row
       float m_run = -INFINITY;                          // running max, log2 units
       float l_run = 0.f;
-      float pv_scale = 1.f;                             // e4m3: dv_max / kP8Scale
-      float dq_s = 0.f, inv_dv_max = 0.f, dk_next = 0.f, dv_next = 0.f;
-      const float *dk_row = nullptr;
-      const float *dv_row = nullptr;
-      if constexpr (C::kFp8) {
-        const size_t base = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
-        dq_s = __ldg(p.dq + base + (row0 >> 7));
-        dk_row = p.dk + base;
-        dv_row = p.dv + base;
-        float dvm = 0.f;
-        for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
-        inv_dv_max = C::kP8Scale / dvm;
-        pv_scale = dvm / C::kP8Scale;
-        dk_next = __ldg(dk_row);
-        dv_next = __ldg(dv_row);
-      }
       for (int j = 0; j < nX; ++j) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
         ++s_cnt;
@@ -575,22 +545,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-        if constexpr (C::kSmemP) {   // S is in registers: the tensor core may overwrite it
-          tc_fence_before();
-          mbar_arrive(&bar_s_free[x]);
-        }
-        // scale of this key block (log2 units per raw score); e4m3: the
-        // block's descales, prefetched one block ahead
-        float cs = p.scale_log2;
-        float pw = 1.f;                                   // e4m3: P prescale
-        if constexpr (C::kFp8) {
-          cs *= dq_s * dk_next;
-          pw = dv_next * inv_dv_max;
-          if (j + 1 < nX) {
-            dk_next = __ldg(dk_row + j + 1);
-            dv_next = __ldg(dv_row + j + 1);
-          }
-        }
+        const float cs = p.scale_log2;   // log2 units per raw score
         const int kbase = j * 128;
         const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
         if (need_mask) {
@@ -600,14 +555,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (kbase + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
-        }
-        // A turn is taken only while no wait has given up: after an abort a
-        // partner hands over at most one more turn (below the tile loop), so
-        // each warp blocks on its turn barrier at most once more.
-        const bool turn = C::kFp8 && j < ti.nA;
-        if (turn) {
-          if (*abort_flag) { ok = false; break; }
-          named_bar_sync(x == 0 ? turn_a : turn_b, 64);
         }
         // row max: four independent chains of three-input maxima
         float mq[4];
@@ -631,80 +578,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float rs = 0.f;
-        uint32_t pbuf = 0;                                // e4m3: P buffer written
-        if constexpr (!C::kFp8) {
-          // x = s * cs - m in packed pairs; four independent packed row sums
-          float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
+        // x = s * cs - m in packed pairs; four independent packed row sums
+        float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              ffma2(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), cs,
-                    cs, -m_use, -m_use);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
-              pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-            }
-            tmem_st16(tS + c * 16, pk);
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), cs, cs,
+                  -m_use, -m_use);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
+            pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
           }
-          rs = ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
-        } else {
-          // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
-          // into the exponent; row sums of the stored values in four packed
-          // fp32 accumulators, divided by pw once per key block
-          const float lpw = __log2f(fmaxf(pw, 1e-30f));
-          const float mb = m_use - lpw;
-          float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float x0, x1, x2, x3;
-              ffma2(x0, x1, __uint_as_float(sr[c][4 * i]), __uint_as_float(sr[c][4 * i + 1]), cs, cs,
-                    -mb, -mb);
-              ffma2(x2, x3, __uint_as_float(sr[c][4 * i + 2]), __uint_as_float(sr[c][4 * i + 3]),
-                    cs, cs, -mb, -mb);
-              const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-              fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
-              fadd2(ra[(i + 2) & 3], rb[(i + 2) & 3], ra[(i + 2) & 3], rb[(i + 2) & 3], p2, p3);
-              pk[c * 8 + i] = pack_e4m3x4(p0, p1, p2, p3);
-            }
-          }
-          rs = (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
-               ex2(-lpw);
-          if (turn) named_bar_arrive(x == 0 ? turn_b : turn_a, 64);
-          // P buffer b = g & 1 (g: P tiles written so far) is free once the
-          // O update that read it two tiles ago has completed; that update
-          // is completion (g >> 1) - 1 of the buffer's barrier.
-          const unsigned g = pstore_cnt++;
-          const uint32_t b = g & 1;
-          pbuf = b;
-          if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[2 * x + b],
-                                                           ((g >> 1) - 1) & 1, wc))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t prow = p_row + b * C::kPTileBytes;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(prow + ((c ^ (r_in & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                         pk[4 * c + 3]);
-          fence_proxy_async_smem();
-          // O_X is rescaled below only after the previous update (tile g - 1,
-          // completion (g - 1) >> 1 of its buffer's barrier) has landed.
-          if (j > 0 && __any_sync(0xffffffffu, resc) &&
-              !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[2 * x + (b ^ 1)],
-                                                 ((g - 1) >> 1) & 1, wc))) {
-            ok = false;
-            break;
-          }
+          tmem_st16(tS + c * 16, pk);
         }
-        l_run += rs;
+        l_run += ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
         // Rescale O after P is stored, when the score row is no longer live
         // (O_X may change until P_X(j) is published; PV_X(j) waits for that).
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -718,20 +608,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(pbuf ? &bar_p_full1[x] : &bar_p_full[x]);
+        mbar_arrive(&bar_p_full[x]);
       }
       if (!ok) break;
       // ---------------- epilogue: O / l, lse ----------------
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_final[x], tcount & 1, wc))) { ok = false; break; }
       tc_fence_after();
       const bool valid = row < ti.L;
-      const float inv_l = (l_run > 0.f) ? pv_scale / l_run : 0.f;
-      using OutT = uint32_t;
-      OutT *orow = nullptr;
+      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      uint32_t *orow = nullptr;
       if (valid) {
         const size_t tok = static_cast<size_t>(ti.start) + row;
-        orow = reinterpret_cast<OutT *>(reinterpret_cast<uint8_t *>(p.o) +
-                                        ((tok * p.H + ti.h) * C::D) * 2);
+        orow = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(p.o) +
+                                            ((tok * p.H + ti.h) * C::D) * 2);
       }
 #pragma unroll
       for (int c = 0; c < C::D / 32; ++c) {
@@ -752,8 +641,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
       if (valid && p.lse != nullptr) {
-        const float lse2 = m_run + __log2f(l_run);
-        const float lse = lse2 * 0.69314718055994531f;
+        const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         if constexpr (C::kVarlen)
           p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
         else
@@ -762,16 +650,200 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar_o_free[x]);
     }
-    // A warp that gave up (a wait ran out) hands its partner one more turn,
-    // so a partner blocked on its turn barrier is released; every other wait
-    // of the partner then sees the abort flag.  Arrivals nobody waits for
-    // are left behind at exit.
-    if (C::kFp8 && !ok) named_bar_arrive(x == 0 ? turn_b : turn_a, 64);
+  } else {
+    // ------------------------------------------------------------------
+    // e4m3 softmax: two threads per query row.  Warp w serves sub-tile
+    // x = (w >> 2) & 1, key half kh = w >> 3 (keys 64 kh .. 64 kh + 63 of
+    // each block, output columns kh D/2 .. kh D/2 + D/2 - 1) and TMEM lane
+    // quarter wq = w & 3; warps w and w ^ 8 hold the same 32 rows and meet at
+    // pair barrier 1 + 4x + wq once per key block to combine their row
+    // maxima (and at the end of a tile their row sums).  Four softmax warps
+    // share each SM sub-partition.
+    // ------------------------------------------------------------------
+    const int x = (warp >> 2) & 1;
+    const int kh = warp >> 3;
+    const int wq = warp & 3;
+    const int r_in = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + x * C::kColS + kh * 64;
+    const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D + kh * (C::D / 2);
+    const uint32_t pair_bar = 1 + x * 4 + wq;
+    // exchange slots: row maxima [2 slots][x][kh][row], row sums [x][kh][row]
+    float *red_max = reinterpret_cast<float *>(smem + C::kOffRed);
+    float *red_sum = red_max + 2 * 2 * 2 * 128;
+    // this thread's 64 bytes of its row of the P tile: 16-byte chunks
+    // 4 kh .. 4 kh + 3, chunk c of row r stored at c ^ (r & 7) (128-byte swizzle)
+    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
+    int s_cnt = 0, tcount = 0;
+    unsigned pstore_cnt = 0;
+    bool ok = true;
+    TileInfo ti;
+    for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+      const int nX = x == 0 ? ti.nA : ti.nB;
+      const int row0 = ti.qt * 256 + x * 128;
+      const int row = row0 + r_in;
+      float m_run = -INFINITY;                          // running max, log2 units
+      float l_run = 0.f;                                // this half's running sum
+      // per-block descales of this (b, h); P is stored as p * pw with
+      // pw = kP8Scale * dv_j / dv_max, undone in the epilogue
+      const size_t dbase = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
+      const float dq_s = __ldg(p.dq + dbase + (row0 >> 7));
+      const float *dk_row = p.dk + dbase;
+      const float *dv_row = p.dv + dbase;
+      float dvm = 0.f;
+      for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
+      const float inv_dv_max = C::kP8Scale / dvm;
+      const float pv_scale = dvm / C::kP8Scale;
+      float dk_next = __ldg(dk_row), dv_next = __ldg(dv_row);
+      bool good = true;   // every wait of this warp so far succeeded
+      for (int j = 0; j < nX; ++j) {
+        good = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc)) && good;
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sv[64];
+        tmem_ld64(tS, sv);
+        // S is in registers: the tensor core may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_s_free[x]);
+        const float cs = p.scale_log2 * dq_s * dk_next;   // log2 units per raw score
+        const float pw = dv_next * inv_dv_max;
+        if (j + 1 < nX) {
+          dk_next = __ldg(dk_row + j + 1);
+          dv_next = __ldg(dv_row + j + 1);
+        }
+        const int kbase = j * 128 + kh * 64;
+        const bool need_mask = (kbase + 64 > ti.L) || (p.causal && kbase + 63 > row0);
+        if (need_mask) {
+          const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
+            if (kbase + 32 + i >= lim) sv[32 + i] = __float_as_uint(-INFINITY);
+          }
+        }
+        float ma = __uint_as_float(sv[0]), mb2 = __uint_as_float(sv[32]);
+#pragma unroll
+        for (int i = 1; i < 31; i += 2) {
+          ma = fmax3(ma, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+          mb2 = fmax3(mb2, __uint_as_float(sv[32 + i]), __uint_as_float(sv[33 + i]));
+        }
+        const float pmax = fmax3(ma, __uint_as_float(sv[31]), fmaxf(mb2, __uint_as_float(sv[63])));
+        // combine the two halves' maxima; the barrier also ANDs the wait
+        // outcomes, so both warps of a pair leave together
+        float *slot = red_max + (j & 1) * 512 + x * 256;
+        slot[kh * 128 + r_in] = pmax;
+        if (!named_bar_and(pair_bar, 64, good)) { ok = false; break; }
+        const float mx = fmaxf(pmax, slot[(kh ^ 1) * 128 + r_in]);
+        const float m_tile = mx * cs;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool resc = m_new > m_run + C::kRescaleThresh;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m_run - m_new);    // 0 when m_run = -inf
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        // The previous O_X update must be complete before O_X is rescaled
+        // and before its P tile is overwritten.
+        if (pstore_cnt > 0)
+          good = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc)) &&
+                 good;
+        ++pstore_cnt;
+        tc_fence_after();
+        // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
+        // into the exponent; row sums of the stored values in packed fp32,
+        // divided by pw once per key block
+        const float lpw = __log2f(fmaxf(pw, 1e-30f));
+        const float mb = m_run - lpw;
+        float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t *sr = sv + 32 * half;
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]), cs, cs, -mb,
+                  -mb);
+            ffma2(x2, x3, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]), cs, cs,
+                  -mb, -mb);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
+            fadd2(ra[(i + 2) & 3], rb[(i + 2) & 3], ra[(i + 2) & 3], rb[(i + 2) & 3], p2, p3);
+            pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          const int c0 = 4 * kh + 2 * half;
+          st_shared_v4(p_row + ((c0 ^ (r_in & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+          st_shared_v4(p_row + (((c0 + 1) ^ (r_in & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+        }
+        fence_proxy_async_smem();
+        l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
+                 ex2(-lpw);
+        // Rescale this half of O_X (the previous update has landed, and
+        // O_X += P_X(j) V_j waits for the arrival below).
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < C::D / 64; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p_full[x]);
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O / l, lse ----------------
+      good = __all_sync(0xffffffffu, mbar_wait(&bar_o_final[x], tcount & 1, wc)) && good;
+      red_sum[(x * 2 + kh) * 128 + r_in] = l_run;
+      if (!named_bar_and(pair_bar, 64, good)) { ok = false; break; }
+      const float l_row = l_run + red_sum[(x * 2 + (kh ^ 1)) * 128 + r_in];
+      tc_fence_after();
+      const bool valid = row < ti.L;
+      const float inv_l = (l_row > 0.f) ? pv_scale / l_row : 0.f;
+      uint32_t *orow = nullptr;
+      if (valid) {
+        const size_t tok = static_cast<size_t>(ti.start) + row;
+        orow = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(p.o) +
+                                            ((tok * p.H + ti.h) * C::D + kh * (C::D / 2)) * 2);
+      }
+#pragma unroll
+      for (int c = 0; c < C::D / 64; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && kh == 0 && p.lse != nullptr) {
+        const float lse = (m_run + __log2f(l_row)) * 0.69314718055994531f;
+        if constexpr (C::kVarlen)
+          p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
+        else
+          p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.N + row] = lse;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_o_free[x]);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == C::kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -113,8 +113,9 @@ def test_fp8_b4_h16_n8192_d128():
     """fp8 e4m3 with block scales and incoherent processing: RMSE against the
     fp64 oracle on the unrotated bf16 inputs <= 1.2e-2 and below the
     per-tensor-scale baseline; lse against the oracle run on the dequantised
-    e4m3 inputs the kernel actually sees within 2^-8 (the relative error of
-    the row sum, which adds f16 exponentials)."""
+    e4m3 inputs the kernel actually sees within 2^-8 (fp32 scores,
+    exponentials and row sums leave far less: this only catches gross
+    errors at the full size; the tight bound is checked at a small size)."""
     w = W.FP8
     x = W.make_inputs(w)
     q, k, v = (x[n].cuda() for n in "qkv")

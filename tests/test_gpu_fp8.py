@@ -116,14 +116,16 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     (the rotation cancels), the error left is the kernel's own:
       * P is stored as e4m3(p * w), w = 32 dv_j / dv_max: relative error
         <= 2^-4 where p*w >= 2^-6 (3 mantissa bits), absolute <= 2^-10 / w
-        below that; the exponential itself is evaluated in f16 pairs
-        (input and result rounding, < 2^-8 relative);
-      * the row sum l adds the f16 exponentials (input and result rounding,
-        ~2^-11 each near the row max) in an f16 tree per 32 keys (at most
-        5 roundings of 2^-11) then in fp32: relative error < 2^-8; O is
-        rounded to bf16 (2^-8 relative).
-    The scores are exact up to fp32 accumulation, so lse = m + log l is off
-    by at most the relative error of l: < 2^-8."""
+        below that; the exponential itself is evaluated in fp32;
+      * the row sum l adds the fp32 exponentials in fp32 (eight partial sums
+        per row); O is rounded to bf16 (2^-8 relative).
+    So |dO| <= 2^-4 A + 2^-8 |O| plus the subnormal term, where A is the
+    attention average of |v|; the test allows (2^-4 + 2^-8) A + 2^-7 |O|.
+    lse = m + log l is fp32 throughout: each score is an fp32 sum of d exact
+    products (error <= d 2^-23 sum_i |q_i k_i| scaled), the exponential has a
+    relative error below 2^-21, and l collects at most N/16 + 8 roundings of
+    2^-24 relative; |dlse| is bounded by the largest score error plus the
+    relative error of l."""
     B, N, H, d = 1, 700, 2, 128
     q, k, v = outlier_qkv(4300, (B, N, H, d))
     signs = random_signs(4300, d)
@@ -132,10 +134,18 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     qd = oracle.dequantize(q8.cpu().numpy(), dq.cpu().numpy())
     kd = oracle.dequantize(k8.cpu().numpy(), dk.cpu().numpy())
     vd = oracle.dequantize(v8.cpu().numpy(), dvn)
-    o_ref, lse_ref = oracle.attention(qd, kd, vd, 1 / math.sqrt(d), False, nthreads=threads())
-    a_ref, _ = oracle.attention(qd, kd, np.abs(vd), 1 / math.sqrt(d), False, nthreads=threads())
-    print(f"fp8 kernel vs oracle on its own inputs: max |dlse| {np.abs(lse - lse_ref).max():.2e}")
-    assert float(np.abs(lse - lse_ref).max()) <= 2.0 ** -8
+    scale = 1 / math.sqrt(d)
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, scale, False, nthreads=threads())
+    a_ref, _ = oracle.attention(qd, kd, np.abs(vd), scale, False, nthreads=threads())
+    # score error bound per row: d 2^-23 scale max_k sum_i |q_i| |k_i|
+    qa = np.abs(qd).transpose(0, 2, 1, 3)                           # [B, H, N, d]
+    ka = np.abs(kd).transpose(0, 2, 1, 3)
+    smax = np.einsum("bhnd,bhmd->bhnm", qa, ka).max(axis=3)         # [B, H, N]
+    lse_tol = d * 2.0 ** -23 * scale * smax + 2.0 ** -21 + (N / 16 + 8) * 2.0 ** -24 + 1e-7
+    dlse = np.abs(lse - lse_ref)
+    print(f"fp8 kernel vs oracle on its own inputs: max |dlse| {dlse.max():.2e} "
+          f"(bound {lse_tol.min():.2e} .. {lse_tol.max():.2e})")
+    assert np.all(dlse <= lse_tol), float((dlse - lse_tol).max())
     # subnormal P: sum_k 2^-10 / w_min |v_k| / l, with l >= 1 (the largest
     # p of a row is at least 2^0)
     w_min = 32.0 * (dvn.min(axis=2) / dvn.max(axis=2))             # [B, H]
