@@ -542,31 +542,28 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        uint32_t sv[128];
+        tmem_ld128(tS, sv);              // the whole score row in one round trip
         const float cs = p.scale_log2;   // log2 units per raw score
         const int kbase = j * 128;
         const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
         if (need_mask) {
           const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (kbase + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 128; ++i)
+            if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
         }
         // row max: four independent chains of three-input maxima
         float mq[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mq[u] = __uint_as_float(sr[u][0]);
+        for (int u = 0; u < 4; ++u) mq[u] = __uint_as_float(sv[32 * u]);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 1; i < 31; i += 2)
-            mq[c] = fmax3(mq[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+            mq[c] = fmax3(mq[c], __uint_as_float(sv[32 * c + i]), __uint_as_float(sv[32 * c + i + 1]));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mq[c] = fmaxf(mq[c], __uint_as_float(sr[c][31]));
+        for (int c = 0; c < 4; ++c) mq[c] = fmaxf(mq[c], __uint_as_float(sv[32 * c + 31]));
         const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
         const float m_tile = mx * cs;
         const float m_new = fmaxf(m_run, m_tile);
@@ -586,14 +583,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), cs, cs,
-                  -m_use, -m_use);
+            ffma2(x0, x1, __uint_as_float(sv[32 * c + 2 * i]), __uint_as_float(sv[32 * c + 2 * i + 1]),
+                  cs, cs, -m_use, -m_use);
             const float p0 = ex2(x0), p1 = ex2(x1);
             fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
             pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
           }
-          tmem_st16(tS + c * 16, pk);
+          tmem_st16_nowait(tS + c * 16, pk);
         }
+        tmem_wait_st();
         l_run += ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
         // Rescale O after P is stored, when the score row is no longer live
         // (O_X may change until P_X(j) is published; PV_X(j) waits for that).
