@@ -101,6 +101,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// A wait that ignores the abort flag: used only to drain our own copies and
+// MMAs before the CTA exits.  Its budget is fixed (about two seconds) and
+// independent of the pipeline-wait budget, so even a run whose waits were
+// made to expire at once lets every copy and MMA land before exit.
+constexpr long long kDrainBudget = 1LL << 32;
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                long long budget = kDrainBudget) {
+  const uint32_t a = smem_addr(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > budget) return;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------

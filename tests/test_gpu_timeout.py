@@ -25,9 +25,26 @@ print("CTX", float(x.sum()))
 """
 
 
-def test_wait_timeout_is_reported_and_context_survives():
+# the 8-bit path: the quantise kernel (double-buffered copies) and the e4m3
+# attention kernel (two softmax warps per row that leave together through
+# their pair barrier)
+CHILD_FP8 = r"""
+import torch
+import attention_forward_softmax_gb300 as agb
+x = torch.randn(2, 2048, 8, 128, device="cuda").to(torch.bfloat16)
+q8, k8, v8, dq, dk, dv = agb.qkv_block_quant_hadamard(x, x, x, None)
+agb.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=False)
+print("STATUS", agb.get_status())
+print("AGAIN", agb.get_status())
+y = torch.ones(16, device="cuda")
+print("CTX", float(y.sum()))
+"""
+
+
+@pytest.mark.parametrize("child", [CHILD, CHILD_FP8], ids=["bf16", "fp8"])
+def test_wait_timeout_is_reported_and_context_survives(child):
     env = dict(os.environ, ATTN_WAIT_BUDGET_CYCLES="1", PYTHONPATH=ROOT)
-    r = subprocess.run([sys.executable, "-c", CHILD], env=env, capture_output=True, text=True,
+    r = subprocess.run([sys.executable, "-c", child], env=env, capture_output=True, text=True,
                        timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr
     assert "STATUS 5" in r.stdout, r.stdout
