@@ -302,6 +302,20 @@ def run_gpu(args):
             "peak_source": peak_note, "kernel_ms": round(attn_ms, 4),
             "algorithmic_flops_per_launch": flops,
             "frac_of_nominal_dense": round(achieved / NOMINAL_DENSE_TFLOPS[dtype], 4)}
+    # secondary roof: the exponential unit.  One exponential per (query,
+    # allowed key) pair = flops / (4 d); the unit evaluates 32 per clock per SM
+    # (ex2.approx.f32 or f16x2 pairs alike, measured on GB300), here at the
+    # median SM clock sampled during the timed region.
+    clk = cs.summary()
+    sm_mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    exps = flops / (4.0 * w.d)
+    mufu_peak = 32.0 * n_sm * sm_mhz * 1e6
+    roof["secondary"] = {"bound": "mufu", "achieved": round(exps / (attn_ms / 1e3) / 1e12, 3),
+                         "peak": round(mufu_peak / 1e12, 3), "unit": "Texp/s",
+                         "frac": round(exps / (attn_ms / 1e3) / mufu_peak, 4),
+                         "peak_source": f"32 exp2 per clock per SM x {n_sm} SMs x "
+                                        f"{sm_mhz:.0f} MHz (median during the timed region)"}
     extra_fields = {}
     if quant_only is not None:
         q_ms = per_launch_ms(quant_only, 20, stream)
