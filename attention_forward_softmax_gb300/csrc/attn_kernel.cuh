@@ -11,12 +11,19 @@
 // How it is laid out on the GPU (our design, not the card's Hopper one):
 //  * one CTA per SM, persistent over work tiles; a work tile is 256 query
 //    rows of one (sequence, head), split into two 128-row sub-tiles A and B;
-//  * warp roles (320 threads; 352 for e4m3):
+//  * warp roles, 16-bit (320 threads):
 //      warps 0-3  softmax warpgroup for sub-tile A (one thread per row)
 //      warps 4-7  softmax warpgroup for sub-tile B
 //      warp  8    MMA issuer (one thread) + TMEM allocation
 //      warp  9    TMA producer (one thread)
-//      warp 10    e4m3 only: second MMA issuer, for the O updates
+//  * warp roles, e4m3 (608 threads):
+//      warps 0-15 softmax, two threads per row: warp w serves sub-tile
+//                 (w >> 2) & 1 and keys 64 (w >> 3) .. 64 (w >> 3) + 63 of
+//                 each block; warps w and w ^ 8 combine their row maxima
+//                 through shared memory at a pair barrier
+//      warp 16    S = Q K^T issuer + TMEM allocation
+//      warp 17    TMA producer
+//      warp 18    O += P V issuer
 //  * Q sub-tiles stay in shared memory for the whole tile; K and V tiles of
 //    128 keys stream through a ring of NS slots (K_0, V_0, K_1, V_1, ...);
 //  * TMEM (512 columns): S_A [0,128), S_B [128,256), O_A, O_B after them;
@@ -36,7 +43,8 @@
 //    exact after the final division by l;
 //  * every mbarrier wait is bounded (clock64 budget): on expiry the kernel
 //    records ATTN_ERR_TIMEOUT in the status word, drains its own copies and
-//    MMAs, frees TMEM and returns.
+//    MMAs, frees TMEM and returns; the e4m3 pair barriers AND their warps'
+//    wait outcomes, so both warps of a pair leave together.
 #pragma once
 
 #include "ptx.cuh"
