@@ -116,13 +116,19 @@ struct Cfg {
   // softmax has read it; 16-bit P stays in TMEM over S.
   static constexpr bool kSmemP = kFp8;
   static constexpr int kPTileBytes = kSmemP ? 128 * 128 : 0;
+  // 16-bit at d = 64: O_A and O_B take only 128 TMEM columns, so P gets its
+  // own 64 columns per sub-tile after them and S is free once it is read,
+  // as in the e4m3 path (P in TMEM rather than shared memory).
+  static constexpr bool kSepP = !kFp8 && D == 64;
+  static constexpr uint32_t kColP0 = 256 + 2 * D;        // kSepP: P_X at kColP0 + 64 x
+  static constexpr bool kDual = kSmemP || kSepP;         // separate S and O issuers
   // e4m3: two softmax threads per query row (16 softmax warps)
   static constexpr bool kSplit = kFp8;
   static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
   static constexpr int kWarpMMA = kSoftmaxWarps;       // MMA issuer (S = Q K^T) + TMEM allocation
   static constexpr int kWarpTMA = kSoftmaxWarps + 1;   // TMA producer
   static constexpr int kWarpPV = kSoftmaxWarps + 2;    // e4m3: second issuer (O += P V)
-  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2 + (kSmemP ? 1 : 0));
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2 + (kDual ? 1 : 0));
   // arrivals per phase on the barriers the softmax signals: one per thread
   // (16-bit), one per warp (e4m3)
   static constexpr int kSoftArrive = kSplit ? 8 : 128;
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&bar_o_final[x], 1);
       mbar_init(&bar_o_free[x], C::kSoftArrive);
     }
-    mbar_init(bar_drain, C::kSmemP ? 2 : 1);
+    mbar_init(bar_drain, C::kDual ? 2 : 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_free[x], C::kSoftArrive);
       mbar_init(&bar_o_done[x], 1);
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (q_issued > 0) mbar_wait_drain(bar_q_full, (q_issued - 1) & 1);
       }
     }
-  } else if (warp == C::kWarpMMA || (C::kSmemP && warp == C::kWarpPV)) {
+  } else if (warp == C::kWarpMMA || (C::kDual && warp == C::kWarpPV)) {
     // ------------------------------------------------------------------
     // MMA issuer(s)
     // ------------------------------------------------------------------
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       auto issue_pv = [&](int x, unsigned pos, bool accumulate, auto &&before_last) {
         const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
         const uint32_t d = tmem + C::kColO0 + x * C::D;
-        const uint32_t pa = tmem + x * C::kColS;
+        const uint32_t pa = tmem + (C::kSepP ? C::kColP0 + x * 64 : x * C::kColS);
         if constexpr (C::kFp8)
           mma_f8_ts(d, pa, desc(va, v_hi), C::kIdescPV, accumulate);
         else
@@ -427,8 +433,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         return true;
       };
 
-      if constexpr (C::kSmemP) {
-        // e4m3: two issuing threads.  Warp 8 issues S_X(j) = Q_X K_j^T as
+      if constexpr (C::kDual) {
+        // e4m3, and 16-bit at d = 64: two issuing threads.  Warp 8 issues S_X(j) = Q_X K_j^T as
         // soon as softmax X has read S_X(j-1); warp 10 issues
         // O_X += P_X(j) V_j as soon as P_X(j) is in shared memory.  Each
         // commit covers only the committing thread's MMAs, so the barrier
@@ -463,7 +469,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                   tc_fence_after();
                 }
                 if (!wait_kv(pv)) { ok = false; break; }
-                issue_pv_smem(0, pv, j > 0);
+                if constexpr (C::kSmemP) issue_pv_smem(0, pv, j > 0);
+                else issue_pv(0, pv, j > 0, no_probe);
                 mma_commit(&bar_o_done[0]);
                 if (j == nA - 1) mma_commit(&bar_o_final[0]);
               }
@@ -473,7 +480,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 tc_fence_after();
               }
               if (j >= nA && !wait_kv(pv)) { ok = false; break; }
-              issue_pv_smem(1, pv, j > 0);
+              if constexpr (C::kSmemP) issue_pv_smem(1, pv, j > 0);
+              else issue_pv(1, pv, j > 0, no_probe);
               mma_commit(&bar_o_done[1]);
               if (j == nB - 1) mma_commit(&bar_o_final[1]);
               mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
@@ -561,7 +569,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + x * C::kColS;
     const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
+    // where P goes: over S, or (d = 64) its own columns
+    const uint32_t tP = C::kSepP ? tmem + lane_base + C::kColP0 + x * 64 : tS;
     int s_cnt = 0, tcount = 0;
+    unsigned pstore_cnt = 0;                 // kSepP: P tiles written so far
     bool ok = true;
     TileInfo ti;
     for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
@@ -576,6 +587,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after();
         uint32_t sv[128];
         tmem_ld128(tS, sv);              // the whole score row in one round trip
+        if constexpr (C::kSepP) {        // S is in registers: the tensor core may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bar_s_free[x]);
+        }
         const float cs = p.scale_log2;   // log2 units per raw score
         const int kbase = j * 128;
         const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
@@ -607,6 +622,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        if constexpr (C::kSepP) {
+          // The previous O_X update must be complete before its P columns are
+          // rewritten and before O_X is rescaled.
+          if (pstore_cnt > 0 &&
+              !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          ++pstore_cnt;
+          tc_fence_after();
+        }
         // x = s * cs - m in packed pairs; four independent packed row sums
         float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -621,7 +647,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
             pk[i] = (C::E == Elem::BF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
           }
-          tmem_st16_nowait(tS + c * 16, pk);
+          tmem_st16_nowait(tP + c * 16, pk);
         }
         tmem_wait_st();
         l_run += ((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]));
