@@ -342,18 +342,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       TileInfo ti;
 
       // S_X = Q_X K^T  (K tile at ring position pos)
-      // `before_last` runs just before the group's last MMA is issued.  The
-      // issue queue holds about one MMA, so a wait placed after a group leaves
-      // the tensor pipe idle for its latency; at d = 64 (short groups) a
-      // non-blocking probe there lets the next group's wait be skipped.
-      auto no_probe = [] {};
-      auto issue_qk = [&](int x, unsigned pos, auto &&before_last) {
+      auto issue_qk = [&](int x, unsigned pos) {
         const uint32_t qa = q_lo + static_cast<uint32_t>(x * (C::kTileBytes >> 4));
         const uint32_t ka = k_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
         const uint32_t d = tmem + x * C::kColS;
 #pragma unroll
         for (int s = 0; s < C::kQKSteps; ++s) {
-          if (s == C::kQKSteps - 1) before_last();
           const uint32_t off = ((s / 4) * C::kChunkBytes + (s % 4) * 32) >> 4;
           if constexpr (C::kFp8)
             mma_f8_ss(d, desc(qa + off, q_hi), desc(ka + off, k_hi), C::kIdescQK, s > 0);
@@ -362,7 +356,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       };
       // O_X (+)= P_X V  (V tile at ring position pos)
-      auto issue_pv = [&](int x, unsigned pos, bool accumulate, auto &&before_last) {
+      auto issue_pv = [&](int x, unsigned pos, bool accumulate) {
         const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
         const uint32_t d = tmem + C::kColO0 + x * C::D;
         const uint32_t pa = tmem + (C::kSepP ? C::kColP0 + x * 64 : x * C::kColS);
@@ -372,7 +366,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mma_f16_ts(d, pa, desc(va, v_hi), C::kIdescPV, accumulate);
 #pragma unroll
         for (int s = 1; s < C::kPVSteps; ++s) {
-          if (s == C::kPVSteps - 1) before_last();
           const uint32_t off = (s * C::kKStep * 128) >> 4;
           if constexpr (C::kFp8)
             mma_f8_ts(d, pa + s * 8, desc(va + off, v_hi), C::kIdescPV, 1);
@@ -406,37 +399,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after();
         return true;
       };
-      constexpr bool kProbe = C::D == 64;   // measured: +4% at d = 64, -1% at d = 128
-      auto probe_kv = [&](unsigned pos) {
-        return kProbe &&
-               mbar_test_wait(smem_addr(&bar_kv_full[pos & (C::NS - 1)]), (pos / C::NS) & 1);
-      };
-      auto wait_kv_after = [&](unsigned pos, bool seen) {
-        if (!seen && !mbar_wait(&bar_kv_full[pos & (C::NS - 1)], (pos / C::NS) & 1, wc))
-          return false;
-        tc_fence_after();
-        return true;
-      };
       auto wait_p = [&](int x) {
         if (!mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
         ++p_cnt[x];
         tc_fence_after();
         return true;
       };
-      auto probe_p = [&](int x) {
-        return kProbe && mbar_test_wait(smem_addr(&bar_p_full[x]), p_cnt[x] & 1);
-      };
-      auto wait_p_after = [&](int x, bool seen) {
-        if (!seen && !mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
-        ++p_cnt[x];
-        tc_fence_after();
-        return true;
-      };
 
       if constexpr (C::kDual) {
-        // e4m3, and 16-bit at d = 64: two issuing threads.  Warp 8 issues S_X(j) = Q_X K_j^T as
-        // soon as softmax X has read S_X(j-1); warp 10 issues
-        // O_X += P_X(j) V_j as soon as P_X(j) is in shared memory.  Each
+        // e4m3, and 16-bit at d = 64: two issuing threads.  Warp kWarpMMA
+        // issues S_X(j) = Q_X K_j^T as soon as softmax X has read S_X(j-1);
+        // warp kWarpPV issues O_X += P_X(j) V_j as soon as P_X(j) is written
+        // (shared memory for e4m3, its own TMEM columns for 16-bit).  Each
         // commit covers only the committing thread's MMAs, so the barrier
         // traffic of one issuer overlaps the other's tensor work.
         const bool qk_role = warp == C::kWarpMMA;
@@ -450,11 +424,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               if (!wait_kv(pk)) { ok = false; break; }
               if (j < nA) {
                 if (!wait_s_free(0)) { ok = false; break; }
-                issue_qk(0, pk, no_probe);
+                issue_qk(0, pk);
                 mma_commit(&bar_s_full[0]);
               }
               if (!wait_s_free(1)) { ok = false; break; }
-              issue_qk(1, pk, no_probe);
+              issue_qk(1, pk);
               mma_commit(&bar_s_full[1]);
               mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
               if (j == nB - 1) mma_commit(bar_q_empty);
@@ -470,7 +444,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 if (!wait_kv(pv)) { ok = false; break; }
                 if constexpr (C::kSmemP) issue_pv_smem(0, pv, j > 0);
-                else issue_pv(0, pv, j > 0, no_probe);
+                else issue_pv(0, pv, j > 0);
                 mma_commit(&bar_o_done[0]);
                 if (j == nA - 1) mma_commit(&bar_o_final[0]);
               }
@@ -481,7 +455,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               }
               if (j >= nA && !wait_kv(pv)) { ok = false; break; }
               if constexpr (C::kSmemP) issue_pv_smem(1, pv, j > 0);
-              else issue_pv(1, pv, j > 0, no_probe);
+              else issue_pv(1, pv, j > 0);
               mma_commit(&bar_o_done[1]);
               if (j == nB - 1) mma_commit(&bar_o_final[1]);
               mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
@@ -494,46 +468,35 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int nA = ti.nA, nB = ti.nB;
         if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        // seen_*: the probe inside the previous MMA group found the barrier
-        // the next group waits for already complete
-        bool seen_k = false;
         for (int j = 0; j < nB; ++j) {
           const unsigned pk = kv_pos + 2 * j, pv = pk + 1;
-          if (!wait_kv_after(pk, seen_k)) { ok = false; break; }
-          bool seen_pb = false;
+          if (!wait_kv(pk)) { ok = false; break; }
           if (j < nA) {
-            issue_qk(0, pk, [&] { if (j >= 1) seen_pb = probe_p(1); });
+            issue_qk(0, pk);
             mma_commit(&bar_s_full[0]);
           }
           if (j >= 1) {   // O_B (+)= P_B(j-1) V_{j-1}
-            if (!wait_p_after(1, seen_pb)) { ok = false; break; }
+            if (!wait_p(1)) { ok = false; break; }
             if (j - 1 == 0) {
               if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
               tc_fence_after();
             }
             if (j - 1 >= nA && !wait_kv(pv - 2)) { ok = false; break; }
-            issue_pv(1, pv - 2, j - 1 > 0, no_probe);
+            issue_pv(1, pv - 2, j - 1 > 0);
             mma_commit(&bar_kv_empty[(pv - 2) & (C::NS - 1)]);
           }
-          bool seen_pa = false, seen_v = false;
-          issue_qk(1, pk, [&] {
-            if (j < nA) {
-              seen_pa = probe_p(0);
-              seen_v = probe_kv(pv);
-            }
-          });
+          issue_qk(1, pk);
           mma_commit(&bar_s_full[1]);
           mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
           if (j == nB - 1) mma_commit(bar_q_empty);
-          seen_k = false;
           if (j < nA) {   // O_A (+)= P_A(j) V_j
-            if (!wait_p_after(0, seen_pa)) { ok = false; break; }
+            if (!wait_p(0)) { ok = false; break; }
             if (j == 0) {
               if (!mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
               tc_fence_after();
             }
-            if (!wait_kv_after(pv, seen_v)) { ok = false; break; }
-            issue_pv(0, pv, j > 0, [&] { if (j + 1 < nB) seen_k = probe_kv(pk + 2); });
+            if (!wait_kv(pv)) { ok = false; break; }
+            issue_pv(0, pv, j > 0);
             if (j == nA - 1) mma_commit(&bar_o_final[0]);
           }
         }
@@ -547,7 +510,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tc_fence_after();
           }
           if (j >= nA && !wait_kv(pv)) { ok = false; break; }
-          issue_pv(1, pv, j > 0, no_probe);
+          issue_pv(1, pv, j > 0);
           mma_commit(&bar_o_final[1]);
           mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
         }
