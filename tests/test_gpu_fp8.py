@@ -155,3 +155,23 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     err = np.abs(o - o_ref)
     assert np.all(err <= tol), float((err - tol).max())
     print(f"fp8 kernel vs oracle on its own inputs: rmse {rmse(o, o_ref):.3e}")
+
+
+def test_fp8_causal_future_keys_are_exactly_masked():
+    """Poison the e4m3 codes of every key at or beyond row r (K = NaN code
+    0x7f, V = +-448 codes 0x7e / 0xfe; the descales are unchanged): outputs of
+    rows < r are bitwise identical to the clean run, so masking is by select
+    in both halves of the two-threads-per-row softmax."""
+    B, N, H, d, r = 2, 400, 2, 128, 190
+    q, k, v = outlier_qkv(4400, (B, N, H, d))
+    q8, k8, v8, dq, dk, dv = agb.qkv_block_quant_hadamard(q.cuda(), k.cuda(), v.cuda(), None)
+    o1, l1 = agb.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=True)
+    kp, vp = k8.clone(), v8.clone()
+    kp[:, r:] = 0x7F
+    vp[:, r:] = 0x7E
+    vp[:, r::2] = 0xFE
+    o2, l2 = agb.attn_fwd_fp8(q8, kp, vp, dq, dk, dv, causal=True)
+    torch.cuda.synchronize()
+    assert agb.get_status() == 0
+    assert torch.equal(o1[:, :r].view(torch.int16), o2[:, :r].view(torch.int16))
+    assert torch.equal(l1[:, :, :r].view(torch.int32), l2[:, :, :r].view(torch.int32))
