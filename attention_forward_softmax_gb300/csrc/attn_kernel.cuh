@@ -11,11 +11,13 @@
 // How it is laid out on the GPU (our design, not the card's Hopper one):
 //  * one CTA per SM, persistent over work tiles; a work tile is 256 query
 //    rows of one (sequence, head), split into two 128-row sub-tiles A and B;
-//  * warp roles, 16-bit (320 threads):
+//  * warp roles, 16-bit (320 threads; 352 at d = 64):
 //      warps 0-3  softmax warpgroup for sub-tile A (one thread per row)
 //      warps 4-7  softmax warpgroup for sub-tile B
-//      warp  8    MMA issuer (one thread) + TMEM allocation
+//      warp  8    MMA issuer (one thread) + TMEM allocation; at d = 64 only
+//                 S = Q K^T, P having its own TMEM columns there
 //      warp  9    TMA producer (one thread)
+//      warp 10    d = 64 only: O += P V issuer
 //  * warp roles, e4m3 (608 threads):
 //      warps 0-15 softmax, two threads per row: warp w serves sub-tile
 //                 (w >> 2) & 1 and keys 64 (w >> 3) .. 64 (w >> 3) + 63 of
