@@ -3,6 +3,8 @@
 // persistent grid of at most one CTA per SM on the caller's stream.
 #pragma once
 
+#include <mutex>
+
 #include "attn_kernel.cuh"
 #include "internal.h"
 
@@ -60,16 +62,19 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   p.status = a.status;
   const int grid = a.num_tiles < a.num_sms ? a.num_tiles : a.num_sms;
   if (grid <= 0) return ATTN_OK;
-  static bool attr_set[64] = {};
+  // The shared-memory attribute is set once per device and instantiation;
+  // concurrent first calls from several host threads are serialised by
+  // call_once.
+  static std::once_flag attr_once[kMaxDevices];
+  static cudaError_t attr_err[kMaxDevices];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(attn_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return ATTN_ERR_LAUNCH;
-    attr_set[dev] = true;
-  }
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::call_once(attr_once[dev], [dev] {
+    attr_err[dev] = cudaFuncSetAttribute(attn_fwd_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  });
+  if (attr_err[dev] != cudaSuccess) return ATTN_ERR_LAUNCH;
   attn_fwd_kernel<C><<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

@@ -8,6 +8,9 @@
 
 namespace attn {
 
+// Devices the per-device host state is kept for (device ordinals 0 .. 63).
+constexpr int kMaxDevices = 64;
+
 // Everything one attention launch needs (already validated).
 struct LaunchArgs {
   const void *q, *k, *v;
@@ -45,7 +48,6 @@ struct DeviceState {
   int2 *tiles = nullptr;        // varlen tile list
   size_t tiles_cap = 0;
   int num_sms = 0;
-  unsigned attr_done = 0;       // bit per kernel instantiation: smem attribute set
 };
 attn_status_t device_state(DeviceState **out);
 

@@ -31,9 +31,8 @@ constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocMaxEntries * sizeof(in
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-constexpr int kMaxDev = 64;
-unsigned char *g_scratch_ptr[kMaxDev] = {};   // device address of g_noalloc_scratch, per device
-int g_num_sms[kMaxDev] = {};
+unsigned char *g_scratch_ptr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
+int g_num_sms[kMaxDevices] = {};
 std::mutex g_setup_mu;
 
 // Once per device, with that device current: look up the device address of
@@ -84,7 +83,7 @@ extern "C" attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, c
     return ATTN_ERR_TOO_LARGE;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   unsigned char *scratch = nullptr;
   int num_sms = 0;
   attn_status_t st = setup(dev, &scratch, &num_sms);

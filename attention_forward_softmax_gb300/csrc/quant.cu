@@ -19,6 +19,7 @@
 // HBM-bound: 2 bytes read and 1 byte written per element.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -291,20 +292,22 @@ extern "C" attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, 
   a.budget = wait_budget();
   const long long items = 3LL * B * H * nblk;
   const int grid = static_cast<int>(std::min<long long>(items, 2LL * ds->num_sms));
-  static bool attr_set[2][64] = {};
+  // shared-memory attribute: once per device and head dimension (call_once
+  // serialises concurrent first calls)
+  static std::once_flag attr_once[2][kMaxDevices];
+  static cudaError_t attr_err[2][kMaxDevices];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (!attr_set[d == 128][dev]) {
-    cudaError_t e = d == 128 ? cudaFuncSetAttribute(quant_kernel<128>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    quant_smem_bytes<128>())
-                             : cudaFuncSetAttribute(quant_kernel<64>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    quant_smem_bytes<64>());
-    if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
-    attr_set[d == 128][dev] = true;
-  }
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  const int di = d == 128 ? 1 : 0;
+  std::call_once(attr_once[di][dev], [di, dev] {
+    attr_err[di][dev] = di ? cudaFuncSetAttribute(quant_kernel<128>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  quant_smem_bytes<128>())
+                           : cudaFuncSetAttribute(quant_kernel<64>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  quant_smem_bytes<64>());
+  });
+  if (attr_err[di][dev] != cudaSuccess) return ATTN_ERR_LAUNCH;
   auto run = [&](int mode) {
     a.mode = mode;
     if (d == 128)

@@ -11,7 +11,6 @@
 namespace attn {
 
 namespace {
-constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 

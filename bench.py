@@ -17,6 +17,14 @@ barrier + synchronize on both sides).  `e2e` repeats the measurement through
 the public API with the inputs copied from pinned host memory and O, lse
 copied back inside the timed region.  `--impl reference` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.
+
+The default line also carries an `fp8` block: the e4m3 workload (B=4 H=16
+N=8192 d=128) with its attention kernel against the fp8 dense peak and its
+quantise pre-step against HBM bandwidth.
+
+`--gpus N` runs N replicas, one rank per GPU.  Under a launcher (WORLD_SIZE
+set) N must equal the number of ranks; without one, the script starts N ranks
+of itself under torch.distributed.run.
 """
 from __future__ import annotations
 
@@ -246,6 +254,55 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def fp8_block(dev, stream, peaks, peak_kind, steps):
+    """The 8-bit workload (e4m3, B=4 H=16 N=8192 d=128, 0.1% outliers) measured
+    beside the default line: the e4m3 attention kernel alone (per-launch CUDA
+    events) against the fp8 dense peak, the quantise pre-step against HBM
+    bandwidth, and the whole step (pre-step + attention)."""
+    import torch
+
+    import attention_forward_softmax_gb300 as agb
+    w = get_workload("fp8")
+    step, _, _, _, _, flops, attn_only, quant_only, bufs = build_step(w, dev)
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    agb.check_status()
+    n = max(10, min(steps, 50))
+    t_step = time_region(step, n, stream)
+    attn_ms = per_launch_ms(attn_only, n, stream)
+    q_ms = per_launch_ms(quant_only, n, stream)
+    agb.check_status()
+    peak = peaks["bf16_tflops"] * 2.0
+    achieved = flops / (attn_ms / 1e3) / 1e12
+    qb = 3 * (bufs[0].numel() * 2 + bufs[0].numel())   # read bf16, write e4m3
+    return {"workload": w.name, "bound": "tensor", "unit": "TFLOP/s",
+            "achieved": round(achieved, 2), "peak": round(peak, 1),
+            "frac": round(achieved / peak, 4),
+            "frac_of_nominal_dense": round(achieved / NOMINAL_DENSE_TFLOPS["e4m3"], 4),
+            "peak_source": f"{peak_kind} bf16 burst x 2 (nominal fp8:bf16 ratio)",
+            "kernel_ms": round(attn_ms, 4), "traffic": traffic_record("fp8"),
+            "step_ms": round(t_step / n * 1e3, 4),
+            "step_tflops": round(flops * n / t_step / 1e12, 2),
+            "quant": {"bound": "hbm", "ms": round(q_ms, 4),
+                      "achieved": round(qb / (q_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": round(qb / (q_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                      "algorithmic_bytes": qb}}
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per launch from profiles/traffic.json, or None once the
+    kernel sources differ from the ones the counters were taken on."""
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tr_path):
+        return None
+    with open(tr_path) as f:
+        rec = json.load(f).get(workload)
+    if rec and rec.get("source_sha") == kernel_source_hash():
+        return rec["bytes"]
+    return None
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -289,14 +346,7 @@ def run_gpu(args):
         peak = peaks["bf16_tflops"]
         peak_note = f"{peak_kind} bf16 burst (cuBLAS)"
     achieved = flops / (attn_ms / 1e3) / 1e12
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            rec = json.load(f).get(args.workload)
-        # counters only count while the kernel sources are the ones measured
-        if rec and rec.get("source_sha") == kernel_source_hash():
-            traffic = rec["bytes"]
+    traffic = traffic_record(args.workload)
     roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": peak_note, "kernel_ms": round(attn_ms, 4),
@@ -326,6 +376,9 @@ def run_gpu(args):
                                  "frac": round(qb / (q_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                  "algorithmic_bytes": qb}
 
+    if args.workload == "dense" and not args.no_fp8:
+        extra_fields["fp8"] = fp8_block(dev, stream, peaks, peak_kind, args.steps)
+
     # end to end through the public API (host buffers)
     for _ in range(2):
         e2e()
@@ -346,7 +399,7 @@ def run_gpu(args):
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(t / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": (round(value / 661.0, 3) if args.workload == "dense" else None),
+            "vs_baseline": None,
             "dtype": dtype, "data": "synthetic (seeded N(0,1)" +
             (", 0.1% N(0,100) outliers" if w.outliers else "") + ")",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
@@ -445,7 +498,8 @@ def run_reference(args):
     threads = oracle.default_threads()
     q, k, v, cu, tok, head = oracle_sample(w, 1 << 16)
     # size one step so that warmup + steps stay within a few minutes
-    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step_budget = args.ref_step_seconds or max(1.0, min(20.0,
+                                                            150.0 / max(1, args.steps + args.warmup)))
     n, _ = calibrate(lambda m: oracle.attention_rows(q, k, v, cu, w.scale, w.causal, tok[:m],
                                                      head[:m], threads), per_step_budget, len(tok))
     for _ in range(max(0, args.warmup - 1)):
@@ -473,6 +527,20 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def relaunch_under_torchrun(args) -> int:
+    """`--gpus N` without a launcher: start N ranks of this script under
+    torch.distributed.run on this node and return its exit status."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr=127.0.0.1",
+           f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,8 +550,20 @@ def main():
                     help="dense | tiny | fp8 | varlen | causal:N:H:d")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="omit the fp8 block of the default (dense) line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: oracle seconds per step (default: sized so the "
+                         "whole run takes a few minutes)")
     args = ap.parse_args()
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        raise SystemExit(relaunch_under_torchrun(args))
+    _, world, _ = rank_info()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but the launcher started {world} ranks")
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)

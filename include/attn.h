@@ -157,7 +157,11 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8,
  *                compared against).
  *   outputs    : q8, k8, v8 [B, N, H, d] e4m3; descale_q/k/v [B, H, ceil(N/128)]
  *                float32 with scale = amax|x| / 448 (1 for an all-zero block),
- *                codes = round-to-nearest-even(x / scale), saturated to +-448.
+ *                codes = round-to-nearest-even(x * (1 / scale)) with x, the
+ *                rotation and the product in float32, saturated to +-448.
+ *                This can differ by one e4m3 step from RNE(x / scale) where
+ *                x / scale lies within a few float32 ulps of a midpoint
+ *                between two codes.
  */
 attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void *v,
                                        void *q8, void *k8, void *v8,

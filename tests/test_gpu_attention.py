@@ -40,8 +40,8 @@ def test_dense_parity_small(N, causal, d, dtype):
     q, k, v = qkv(2000 + N + d, (B, N, H, d), dtype)
     scale = 1.0 / math.sqrt(d)
     o, lse = run_dense(q, k, v, causal)
-    o_ref, lse_ref, a_ref = oracle_dense(q, k, v, scale, causal)
-    assert_close_o(o, o_ref, a_ref, dtype, f"N={N} d={d} causal={causal}")
+    o_ref, lse_ref, a_ref, ne = oracle_dense(q, k, v, scale, causal)
+    assert_close_o(o, o_ref, a_ref, dtype, ne, f"N={N} d={d} causal={causal}")
     assert_close_lse(lse, lse_ref, f"N={N} d={d} causal={causal}")
 
 
@@ -50,8 +50,8 @@ def test_tiny_config_b1_h1_n128_d64():
     from datagen.workloads import TINY, make_inputs
     x = make_inputs(TINY)
     o, lse = run_dense(x["q"], x["k"], x["v"], False)
-    o_ref, lse_ref, a_ref = oracle_dense(x["q"], x["k"], x["v"], TINY.scale, False)
-    assert_close_o(o, o_ref, a_ref, torch.bfloat16, "tiny")
+    o_ref, lse_ref, a_ref, ne = oracle_dense(x["q"], x["k"], x["v"], TINY.scale, False)
+    assert_close_o(o, o_ref, a_ref, torch.bfloat16, ne, "tiny")
     # this configuration sits in the regime of the 2e-3 bar itself
     assert np.abs(o - o_ref).max() <= 2e-3
     assert_close_lse(lse, lse_ref, "tiny")
@@ -64,8 +64,10 @@ def test_dense_multi_tile_persistent(d, causal):
     B, H, N = 3, 64, 600
     q, k, v = qkv(2100 + d, (B, N, H, d), torch.bfloat16)
     o, lse = run_dense(q, k, v, causal)
-    o_ref, lse_ref, a_ref = oracle_dense(q, k, v, 1 / math.sqrt(d), causal)
-    assert_close_o(o, o_ref, a_ref, torch.bfloat16, "multi-tile")
+    o_ref, lse_ref, a_ref, ne = oracle_dense(q, k, v, 1 / math.sqrt(d), causal)
+    strict = assert_close_o(o, o_ref, a_ref, torch.bfloat16, ne, "multi-tile")
+    # non-causal rows average 600 keys: nearly every element meets the bare bar
+    assert causal or strict > 0.99
     assert_close_lse(lse, lse_ref, "multi-tile")
 
 
@@ -81,8 +83,8 @@ def test_varlen_parity(causal, d):
     o, lse = agb.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_d, max(lens), causal=causal)
     torch.cuda.synchronize()
     assert agb.get_status() == 0
-    o_ref, lse_ref, a_ref = oracle_varlen(q, k, v, cu, 1 / math.sqrt(d), causal)
-    assert_close_o(o.float().cpu().numpy(), o_ref, a_ref, torch.bfloat16, "varlen")
+    o_ref, lse_ref, a_ref, ne = oracle_varlen(q, k, v, cu, 1 / math.sqrt(d), causal)
+    assert_close_o(o.float().cpu().numpy(), o_ref, a_ref, torch.bfloat16, ne, "varlen")
     assert_close_lse(lse.cpu().numpy(), lse_ref, "varlen")
 
 
@@ -162,8 +164,8 @@ def test_lse_optional_and_custom_scale():
     o, lse = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=0.3, want_lse=False)
     torch.cuda.synchronize()
     assert lse is None
-    o_ref, _, a_ref = oracle_dense(q, k, v, 0.3, False)
-    assert_close_o(o.float().cpu().numpy(), o_ref, a_ref, torch.bfloat16, "scale 0.3")
+    o_ref, _, a_ref, ne = oracle_dense(q, k, v, 0.3, False)
+    assert_close_o(o.float().cpu().numpy(), o_ref, a_ref, torch.bfloat16, ne, "scale 0.3")
 
 
 def test_malformed_cu_seqlens_reported():

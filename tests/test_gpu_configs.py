@@ -9,7 +9,7 @@ import torch
 import attention_forward_softmax_gb300 as agb
 import oracle
 from datagen import workloads as W
-from tests._gpu_helpers import TOL_LSE, TOL_O, o_tolerance, threads
+from tests._gpu_helpers import TOL_LSE, TOL_O, n_eff, o_tolerance, threads
 
 pytestmark = pytest.mark.gpu
 
@@ -39,11 +39,14 @@ def sample(w, count, seed):
 
 
 def oracle_rows(w, x, toks, heads):
+    """(O, lse, A, n_eff) of the sampled rows: A on |V| and the effective key
+    count from the lse at twice the scale, for the tolerance."""
     q, k, v = (x[n].to(torch.float64).numpy().reshape(w.tokens, w.H, w.d) for n in "qkv")
     cu = w.cu_seqlens()
     o, lse = oracle.attention_rows(q, k, v, cu, w.scale, w.causal, toks, heads, threads())
     a, _ = oracle.attention_rows(q, k, np.abs(v), cu, w.scale, w.causal, toks, heads, threads())
-    return o, lse, a
+    _, lse2 = oracle.attention_rows(q, k, v, cu, 2.0 * w.scale, w.causal, toks, heads, threads())
+    return o, lse, a, n_eff(lse, lse2)[:, None]
 
 
 def gpu_rows(w, o, lse, toks, heads):
@@ -69,26 +72,21 @@ def run_16bit(w, x):
     return o, lse
 
 
-def check(w, count, seed, strict_min_keys=None):
+def check(w, count, seed):
     x = W.make_inputs(w)
     o, lse = run_16bit(w, x)
     toks, heads = sample(w, count, seed)
     og, lg = gpu_rows(w, o, lse, toks, heads)
-    o_ref, lse_ref, a_ref = oracle_rows(w, x, toks, heads)
+    o_ref, lse_ref, a_ref, ne = oracle_rows(w, x, toks, heads)
     err = np.abs(og - o_ref)
-    tol = o_tolerance(o_ref, a_ref, torch.bfloat16)
+    tol = o_tolerance(o_ref, a_ref, torch.bfloat16, ne)
+    strict = tol == TOL_O
     dlse = float(np.abs(lg - lse_ref).max())
-    print(f"{w.name}: {len(toks)} sampled rows, max |dO| {err.max():.3e}, max |dlse| {dlse:.3e}")
+    print(f"{w.name}: {len(toks)} sampled rows, max |dO| {err.max():.3e} (held to the bare "
+          f"2e-3: {strict.mean():.1%} of elements, max there {err[strict].max():.3e}), "
+          f"max |dlse| {dlse:.3e}")
     assert np.all(err <= tol), f"{w.name}: max |dO| {err.max():.3e}"
     assert dlse <= TOL_LSE
-    if strict_min_keys is not None:
-        # rows that average many keys meet the 2e-3 bar itself
-        cu = w.cu_seqlens()
-        seq = np.searchsorted(cu, toks, side="right") - 1
-        pos = toks - cu[seq]
-        nkeys = (pos + 1) if w.causal else (cu[seq + 1] - cu[seq])
-        many = nkeys >= strict_min_keys
-        assert err[many].max() <= TOL_O, f"{w.name}: max |dO| {err[many].max():.3e}"
     return float(err.max())
 
 
@@ -97,27 +95,28 @@ def test_tiny_b1_h1_n128_d64():
 
 
 def test_dense_b4_h16_n8448_d128():
-    check(W.DENSE, 512, 2, strict_min_keys=1)
+    check(W.DENSE, 512, 2)
 
 
 @pytest.mark.parametrize("w", W.causal_sweep(), ids=lambda w: f"N{w.N}_H{w.H}_d{w.d}")
 def test_causal_sweep(w):
-    check(w, 256, 4, strict_min_keys=512)
+    check(w, 256, 4)
 
 
 def test_varlen_causal_32_sequences():
     w = W.varlen_causal()
     assert len(w.lengths) == 32 and min(w.lengths) >= 64 and max(w.lengths) <= 4096
-    check(w, 512, 5, strict_min_keys=512)
+    check(w, 512, 5)
 
 
 def test_fp8_b4_h16_n8192_d128():
-    """fp8 e4m3 with block scales and incoherent processing: RMSE against the
-    fp64 oracle on the unrotated bf16 inputs <= 1.2e-2 and below the
-    per-tensor-scale baseline; lse against the oracle run on the dequantised
-    e4m3 inputs the kernel actually sees within 2^-8 (fp32 scores,
-    exponentials and row sums leave far less: this only catches gross
-    errors at the full size; the tight bound is checked at a small size)."""
+    """fp8 e4m3 with block scales and incoherent processing: RMSE over every
+    output element against the fp64 oracle on the unrotated bf16 inputs
+    <= 1.2e-2 and below the per-tensor-scale baseline; lse against the oracle
+    run on the dequantised e4m3 inputs the kernel actually sees within 2^-8
+    on sampled rows (fp32 scores, exponentials and row sums leave far less:
+    this only catches gross errors at the full size; the tight bound is
+    checked at a small size)."""
     w = W.FP8
     x = W.make_inputs(w)
     q, k, v = (x[n].cuda() for n in "qkv")
@@ -128,22 +127,24 @@ def test_fp8_b4_h16_n8192_d128():
         o, lse = agb.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=False)
         torch.cuda.synchronize()
         assert agb.get_status() == 0
-        outs[name] = (o, lse, [t.cpu().numpy() for t in (q8, k8, v8, dq, dk, dv)])
-    toks, heads = sample(w, 512, 3)
-    o_ref, lse_ref, _ = oracle_rows(w, x, toks, heads)
+        outs[name] = (o.float().cpu().numpy(), lse.cpu().numpy(),
+                      [t.cpu().numpy() for t in (q8, k8, v8, dq, dk, dv)])
+    # the whole output of the oracle (4 x 16 x 8192 rows, about 2.2e12 flops)
+    o_ref, _ = oracle.attention(x["q"], x["k"], x["v"], w.scale, False, nthreads=threads())
     r = {}
     for name, (o, lse, _) in outs.items():
-        og, lg = gpu_rows(w, o, lse, toks, heads)
-        assert np.isfinite(og).all() and np.isfinite(lg).all()
-        r[name] = float(np.sqrt(np.mean((og - o_ref) ** 2)))
-    print(f"fp8 RMSE vs fp64: block+rotation {r['block']:.4e}, per-tensor {r['per_tensor']:.4e}")
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        r[name] = float(np.sqrt(np.mean((o - o_ref) ** 2)))
+    print(f"fp8 RMSE vs fp64 over all {o_ref.size} elements: block+rotation {r['block']:.4e}, "
+          f"per-tensor {r['per_tensor']:.4e}")
     assert r["block"] <= 1.2e-2, r
     assert r["block"] < r["per_tensor"], r
-    # the kernel on its own (dequantised) inputs
+    # the kernel on its own (dequantised) inputs, sampled rows
+    toks, heads = sample(w, 512, 3)
     o, lse, (q8, k8, v8, dq, dk, dv) = outs["block"]
     qd, kd, vd = (oracle.dequantize(c, s).reshape(w.tokens, w.H, w.d)
                   for c, s in ((q8, dq), (k8, dk), (v8, dv)))
     _, lse_deq = oracle.attention_rows(qd, kd, vd, w.cu_seqlens(), w.scale, False, toks, heads,
                                        threads())
-    _, lg = gpu_rows(w, o, lse, toks, heads)
-    assert float(np.abs(lg - lse_deq).max()) <= 2.0 ** -8
+    b, n = toks // w.N, toks % w.N
+    assert float(np.abs(lse[b, heads, n] - lse_deq).max()) <= 2.0 ** -8

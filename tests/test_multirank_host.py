@@ -60,18 +60,42 @@ def _bench(env_extra, *args):
 
 
 def test_reference_arm_other_ranks_exit_quietly():
-    r = _bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--impl", "reference",
+    r = _bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--gpus", "2", "--impl",
+               "reference",
                "--steps", "1", "--warmup", "1", "--workload", "tiny")
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
 
 
 def test_reference_arm_rank0_prints_one_json_line():
-    r = _bench({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}, "--impl", "reference",
-               "--steps", "1", "--warmup", "1", "--workload", "tiny")
+    r = _bench({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}, "--gpus", "2", "--impl",
+               "reference", "--steps", "1", "--warmup", "1", "--workload", "tiny",
+               "--ref-step-seconds", "1")
     assert r.returncode == 0, r.stderr
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself, so the
+    line reports the job's two replicas (reference arm: rank 0 prints)."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--steps", "1", "--warmup", "0",
+                        "--workload", "tiny", "--ref-step-seconds", "1"],
+                       env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_the_launcher():
+    r = _bench({"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"}, "--gpus", "2", "--impl",
+               "reference", "--steps", "1", "--warmup", "0", "--workload", "tiny")
+    assert r.returncode != 0
+    assert "--gpus 2" in r.stderr
