@@ -12,6 +12,15 @@ What each function restates:
     "Fused attention kernel" (wikillm concept card), Overview and
     Implementation sketch: O = softmax(scale * Q K^T) V per sequence (causal:
     top-left aligned), lse = M + log Z in natural-log units;
+  * :func:`attention_rows_gqa`, :func:`attention_gqa`,
+    :func:`attention_varlen_gqa`, :func:`attention_paged` -- the same
+    definition for the inference variants (HippoAttention case study,
+    streamhpc.com, "Our approach": paged attention; FlashAttention-3 summary,
+    arxivlens, Limitations: LLM inference): grouped K/V heads, query and key
+    sequences of different lengths (causal: queries at the end), keys read
+    through a page table;
+  * :func:`merge_partials` -- the combination of softmax results over
+    disjoint key sets (split-key decoding), written out from the definition;
   * :func:`rotate`, :func:`hadamard_matrix` -- incoherent processing, same card,
     "8-bit forward pass (FP8, Hopper)": x -> x * diag(signs) * H_d / sqrt(d);
   * :func:`e4m3_encode`, :func:`e4m3_decode`, :func:`block_quant`,
@@ -66,6 +75,12 @@ def _load():
             _dp, _dp, _dp, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_double, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp, _dp,
             ctypes.c_int32]
+        lib.oracle_attention_rows_gqa.argtypes = [
+            _dp, _dp, _dp, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_double, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp,
+            _dp, ctypes.c_int32]
+        lib.oracle_merge_partials.argtypes = [_dp, _dp, ctypes.c_int32, ctypes.c_int64,
+                                              ctypes.c_int32, _dp, _dp]
         lib.oracle_attention_probs.argtypes = [
             _dp, _dp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
             ctypes.c_int32, _dp]
@@ -141,6 +156,104 @@ def attention(q, k, v, scale: float, causal: bool, nthreads=None):
     o, lse = attention_varlen(q.reshape(B * N, H, d), _f64(k).reshape(B * N, H, d),
                               _f64(v).reshape(B * N, H, d), cu, scale, causal, nthreads)
     return o.reshape(B, N, H, d), lse.reshape(H, B, N).transpose(1, 0, 2).copy()
+
+
+def attention_rows_gqa(q, k, v, cu_q, cu_k, scale: float, causal: bool, row_tok, row_head,
+                       nthreads: int | None = None):
+    """O [nrows, d] and lse [nrows] with separate query / key sequences and
+    grouped K/V heads: q [Tq, H, d], k, v [Tk, Hkv, d]; sequence s holds
+    queries cu_q[s]..cu_q[s+1]-1 and keys cu_k[s]..cu_k[s+1]-1; query head h
+    uses K/V head h // (H // Hkv); causal: the queries are the last Lq of the
+    Lk positions (query i sees keys j <= i + Lk - Lq)."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, H, d = q.shape
+    Hkv = k.shape[1]
+    cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+    ck = np.ascontiguousarray(cu_k, dtype=np.int32)
+    rt = np.ascontiguousarray(row_tok, dtype=np.int64)
+    rh = np.ascontiguousarray(row_head, dtype=np.int32)
+    n = rt.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_attention_rows_gqa(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
+                                       _ptr(cq, _i32p), _ptr(ck, _i32p), len(cq) - 1, H, Hkv, d,
+                                       float(scale), int(bool(causal)), _ptr(rt, _i64p),
+                                       _ptr(rh, _i32p), n, _ptr(o, _dp), _ptr(lse, _dp),
+                                       nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows_gqa failed ({rc})")
+    return o, lse
+
+
+def attention_varlen_gqa(q, k, v, cu_q, cu_k, scale: float, causal: bool, nthreads=None):
+    """Full O [Tq, H, d] and lse [H, Tq] for packed query / key sequences
+    with grouped K/V heads (see attention_rows_gqa)."""
+    q = _f64(q)
+    Tq, H, d = q.shape
+    tok = np.repeat(np.arange(Tq, dtype=np.int64), H)
+    head = np.tile(np.arange(H, dtype=np.int32), Tq)
+    o, lse = attention_rows_gqa(q, k, v, cu_q, cu_k, scale, causal, tok, head, nthreads)
+    return o.reshape(Tq, H, d), lse.reshape(Tq, H).T.copy()
+
+
+def attention_gqa(q, k, v, scale: float, causal: bool, nthreads=None):
+    """Dense O [B, Nq, H, d] and lse [B, H, Nq] for q [B, Nq, H, d] and
+    k, v [B, Nk, Hkv, d] (causal: the queries are the last Nq positions)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Nq, H, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    cq = (np.arange(B + 1) * Nq).astype(np.int32)
+    ck = (np.arange(B + 1) * Nk).astype(np.int32)
+    o, lse = attention_varlen_gqa(q.reshape(B * Nq, H, d), k.reshape(B * Nk, Hkv, d),
+                                  v.reshape(B * Nk, Hkv, d), cq, ck, scale, causal, nthreads)
+    return o.reshape(B, Nq, H, d), lse.reshape(H, B, Nq).transpose(1, 0, 2).copy()
+
+
+def gather_pages(cache, block_table, seqlens):
+    """The keys (or values) of each sequence of a paged cache, packed:
+    cache [num_pages, page_size, Hkv, d]; token t of sequence b is row
+    t % page_size of page block_table[b][t // page_size].  Returns
+    ([sum(seqlens), Hkv, d], cu) with cu the key offsets."""
+    cache = np.asarray(cache)
+    P = cache.shape[1]
+    rows = []
+    for b, L in enumerate(seqlens):
+        t = np.arange(int(L))
+        rows.append(cache[np.asarray(block_table[b])[t // P], t % P])
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    return np.concatenate(rows, axis=0), cu
+
+
+def attention_paged(q, k_cache, v_cache, block_table, seqlens_k, scale: float, causal: bool,
+                    nthreads=None):
+    """O [B, Nq, H, d] and lse [B, H, Nq] of queries q [B, Nq, H, d] against a
+    paged K/V cache (see gather_pages); causal: the Nq queries are the last
+    Nq of the seqlens_k[b] positions."""
+    q = _f64(q)
+    B, Nq, H, d = q.shape
+    kp, ck = gather_pages(_f64(k_cache), block_table, seqlens_k)
+    vp, _ = gather_pages(_f64(v_cache), block_table, seqlens_k)
+    cq = (np.arange(B + 1) * Nq).astype(np.int32)
+    o, lse = attention_varlen_gqa(q.reshape(B * Nq, H, d), kp, vp, cq, ck, scale, causal,
+                                  nthreads)
+    return o.reshape(B, Nq, H, d), lse.reshape(H, B, Nq).transpose(1, 0, 2).copy()
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine results over disjoint key sets of the same rows:
+    o_parts [S, R, d], lse_parts [S, R] -> (o [R, d], lse [R]) with
+    lse = log sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s."""
+    lib = _load()
+    op = _f64(o_parts)
+    lp = _f64(lse_parts)
+    S, R, d = op.shape
+    o = np.empty((R, d), dtype=np.float64)
+    lse = np.empty(R, dtype=np.float64)
+    if lib.oracle_merge_partials(_ptr(op, _dp), _ptr(lp, _dp), S, R, d, _ptr(o, _dp),
+                                 _ptr(lse, _dp)) != 0:
+        raise ValueError("oracle_merge_partials failed")
+    return o, lse
 
 
 def probs(q, k, scale: float, causal: bool):

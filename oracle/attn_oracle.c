@@ -44,8 +44,8 @@
 
 typedef struct {
     const double *q, *k, *v;
-    const int32_t *cu;
-    int32_t nseq, H, d, causal;
+    const int32_t *cu, *cuk;
+    int32_t nseq, H, Hkv, d, causal;
     double scale;
     const int64_t *row_tok;
     const int32_t *row_head;
@@ -69,11 +69,12 @@ static int32_t seq_of(const int32_t *cu, int32_t nseq, int64_t t)
 static void *rows_worker(void *arg)
 {
     rows_job *jb = (rows_job *)arg;
-    const int32_t H = jb->H, d = jb->d;
-    const int64_t tok_stride = (int64_t)H * d;
+    const int32_t H = jb->H, Hkv = jb->Hkv, d = jb->d;
+    const int64_t tok_stride = (int64_t)H * d;       /* q rows */
+    const int64_t kv_stride = (int64_t)Hkv * d;      /* k, v rows */
     int64_t maxlen = 0;
     for (int32_t s = 0; s < jb->nseq; ++s) {
-        int64_t L = (int64_t)jb->cu[s + 1] - jb->cu[s];
+        int64_t L = (int64_t)jb->cuk[s + 1] - jb->cuk[s];
         if (L > maxlen) maxlen = L;
     }
     double *sc = (double *)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
@@ -85,16 +86,23 @@ static void *rows_worker(void *arg)
         double *orow = jb->o + r * d;
         const int32_t s = seq_of(jb->cu, jb->nseq, t);
         if (s < 0 || h < 0 || h >= H) { jb->status = -1; break; }
-        const int64_t start = jb->cu[s];
-        const int64_t L = (int64_t)jb->cu[s + 1] - start;
-        const int64_t i = t - start;                 /* position in its sequence */
-        const int64_t nkeys = jb->causal ? i + 1 : L; /* allowed keys j < nkeys */
+        const int64_t i = t - jb->cu[s];             /* position among its queries */
+        const int64_t Lq = (int64_t)jb->cu[s + 1] - jb->cu[s];
+        const int64_t kstart = jb->cuk[s];
+        const int64_t Lk = (int64_t)jb->cuk[s + 1] - kstart;
+        /* allowed keys j < nkeys: all of them, or (causal) those at or before
+           the query's position when the queries are the last Lq of the Lk
+           positions -- j <= i + Lk - Lq, which is j <= i when Lq = Lk */
+        int64_t nkeys = jb->causal ? i + 1 + (Lk - Lq) : Lk;
+        if (nkeys > Lk) nkeys = Lk;
+        if (nkeys < 0) nkeys = 0;
+        const int32_t hk = h / (H / Hkv);           /* the K/V head of query head h */
 
         const double *qrow = jb->q + t * tok_stride + (int64_t)h * d;
         /* scores s_j = scale * sum_c q_c k_jc, and their maximum */
         double mx = -INFINITY;
         for (int64_t j = 0; j < nkeys; ++j) {
-            const double *krow = jb->k + (start + j) * tok_stride + (int64_t)h * d;
+            const double *krow = jb->k + (kstart + j) * kv_stride + (int64_t)hk * d;
             double acc = 0.0;
             for (int32_t c = 0; c < d; ++c) acc += qrow[c] * krow[c];
             sc[j] = jb->scale * acc;
@@ -110,7 +118,7 @@ static void *rows_worker(void *arg)
         for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
         for (int64_t j = 0; j < nkeys; ++j) {
             const double w = exp(sc[j] - mx);
-            const double *vrow = jb->v + (start + j) * tok_stride + (int64_t)h * d;
+            const double *vrow = jb->v + (kstart + j) * kv_stride + (int64_t)hk * d;
             z += w;
             for (int32_t c = 0; c < d; ++c) orow[c] += w * vrow[c];
         }
@@ -122,22 +130,26 @@ static void *rows_worker(void *arg)
 }
 
 /*
- * O and LSE for the query rows (row_tok[r], row_head[r]), r < nrows.
- * q, k, v: packed [T, H, d] (token-major); sequence s holds tokens
- * cu_seqlens[s] .. cu_seqlens[s+1]-1.  A dense [B, N, H, d] batch is the
- * same bytes with cu_seqlens = 0, N, 2N, ...
+ * O and LSE for the query rows (row_tok[r], row_head[r]), r < nrows, with
+ * separate query and key sequences and grouped K/V heads.
+ * q: packed [Tq, H, d]; k, v: packed [Tk, Hkv, d] (token-major).  Sequence s
+ * holds queries cu_q[s] .. cu_q[s+1]-1 and keys cu_k[s] .. cu_k[s+1]-1.
+ * Query head h uses K/V head h / (H / Hkv) (Hkv divides H).  Causal: the
+ * queries of a sequence are its last Lq positions, so query i sees keys
+ * j <= i + Lk - Lq (top-left j <= i when Lq = Lk); a query with no allowed
+ * key gets O = 0, lse = -inf.
  * o: [nrows, d]; lse: [nrows].
  */
-int oracle_attention_rows(const double *q, const double *k, const double *v,
-                          const int32_t *cu_seqlens, int32_t nseq,
-                          int32_t H, int32_t d, double scale, int32_t causal,
-                          const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
-                          double *o, double *lse, int32_t nthreads)
+int oracle_attention_rows_gqa(const double *q, const double *k, const double *v,
+                              const int32_t *cu_q, const int32_t *cu_k, int32_t nseq,
+                              int32_t H, int32_t Hkv, int32_t d, double scale, int32_t causal,
+                              const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
+                              double *o, double *lse, int32_t nthreads)
 {
-    if (!q || !k || !v || !cu_seqlens || !row_tok || !row_head || !o || !lse) return -1;
-    if (nseq < 1 || H < 1 || d < 1 || nrows < 0) return -1;
+    if (!q || !k || !v || !cu_q || !cu_k || !row_tok || !row_head || !o || !lse) return -1;
+    if (nseq < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || nrows < 0) return -1;
     for (int32_t s = 0; s < nseq; ++s)
-        if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+        if (cu_q[s + 1] < cu_q[s] || cu_k[s + 1] < cu_k[s]) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if ((int64_t)nthreads > nrows) nthreads = nrows > 0 ? (int32_t)nrows : 1;
@@ -146,8 +158,8 @@ int oracle_attention_rows(const double *q, const double *k, const double *v,
     pthread_t th[256];
     for (int32_t w = 0; w < nthreads; ++w) {
         rows_job *jb = &jobs[w];
-        jb->q = q; jb->k = k; jb->v = v; jb->cu = cu_seqlens; jb->nseq = nseq;
-        jb->H = H; jb->d = d; jb->causal = causal; jb->scale = scale;
+        jb->q = q; jb->k = k; jb->v = v; jb->cu = cu_q; jb->cuk = cu_k; jb->nseq = nseq;
+        jb->H = H; jb->Hkv = Hkv; jb->d = d; jb->causal = causal; jb->scale = scale;
         jb->row_tok = row_tok; jb->row_head = row_head;
         jb->r0 = nrows * w / nthreads; jb->r1 = nrows * (w + 1) / nthreads;
         jb->o = o; jb->lse = lse; jb->status = 0;
@@ -163,6 +175,56 @@ int oracle_attention_rows(const double *q, const double *k, const double *v,
         if (jobs[w].status < 0) status = jobs[w].status;
     }
     return status;
+}
+
+/*
+ * O and LSE for the query rows (row_tok[r], row_head[r]), r < nrows.
+ * q, k, v: packed [T, H, d] (token-major); sequence s holds tokens
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1 (as queries and as keys).  A dense
+ * [B, N, H, d] batch is the same bytes with cu_seqlens = 0, N, 2N, ...
+ * o: [nrows, d]; lse: [nrows].
+ */
+int oracle_attention_rows(const double *q, const double *k, const double *v,
+                          const int32_t *cu_seqlens, int32_t nseq,
+                          int32_t H, int32_t d, double scale, int32_t causal,
+                          const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
+                          double *o, double *lse, int32_t nthreads)
+{
+    return oracle_attention_rows_gqa(q, k, v, cu_seqlens, cu_seqlens, nseq, H, H, d, scale,
+                                     causal, row_tok, row_head, nrows, o, lse, nthreads);
+}
+
+/*
+ * Merge of partial results over disjoint key sets of the same query rows
+ * (the combine step of attention split over key ranges): with lse_s and
+ * O_s the results over part s,
+ *   lse = log sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
+ * A part with no keys (lse_s = -inf) contributes nothing.
+ * o_parts: [nparts, nrows, d]; lse_parts: [nparts, nrows]; o: [nrows, d];
+ * lse: [nrows].
+ */
+int oracle_merge_partials(const double *o_parts, const double *lse_parts, int32_t nparts,
+                          int64_t nrows, int32_t d, double *o, double *lse)
+{
+    if (!o_parts || !lse_parts || !o || !lse || nparts < 1 || nrows < 0 || d < 1) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        double mx = -INFINITY;
+        for (int32_t s = 0; s < nparts; ++s)
+            if (lse_parts[(int64_t)s * nrows + r] > mx) mx = lse_parts[(int64_t)s * nrows + r];
+        double *orow = o + r * d;
+        for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+        if (mx == -INFINITY) { lse[r] = -INFINITY; continue; }
+        double z = 0.0;
+        for (int32_t s = 0; s < nparts; ++s) {
+            const double w = exp(lse_parts[(int64_t)s * nrows + r] - mx);
+            const double *op = o_parts + ((int64_t)s * nrows + r) * d;
+            z += w;
+            for (int32_t c = 0; c < d; ++c) orow[c] += w * op[c];
+        }
+        for (int32_t c = 0; c < d; ++c) orow[c] /= z;
+        lse[r] = mx + log(z);
+    }
+    return 0;
 }
 
 /*

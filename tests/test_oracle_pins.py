@@ -371,3 +371,121 @@ def test_quantize_qkv_rotates_q_and_k_only():
     s_ref = np.einsum("nc,mc->nm", q[0, :, 0], k[0, :, 0])
     s_q = np.einsum("nc,mc->nm", qd[0, :, 0], kd[0, :, 0])
     assert np.sqrt(np.mean((s_q - s_ref) ** 2)) < 0.1 * np.sqrt(np.mean(s_ref ** 2))
+
+
+# --------------------------------------------------------------------------
+# Inference variants: grouped K/V heads, queries at the end of the keys,
+# paged keys, and the merge of partial results over key ranges
+# (HippoAttention case study, "Our approach": paged attention;
+# FlashAttention-3 summary, Limitations: LLM inference)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("hkv", [1, 2, 4])
+def test_gqa_matches_torch_sdpa_float64(hkv, causal):
+    """Grouped K/V heads against torch's own grouped-query SDPA in float64
+    (catches a wrong head mapping, e.g. h % Hkv instead of h // (H/Hkv))."""
+    B, N, H, d = 2, 19, 8, 16
+    q, k, v = rnd(50, (B, N, H, d)), rnd(50, (B, N, hkv, d), 1), rnd(50, (B, N, hkv, d), 2)
+    o, lse = oracle.attention_gqa(q, k, v, 0.3, causal)
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                           scale=0.3, enable_gqa=True)
+    np.testing.assert_allclose(o, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    # lse against an explicit log-sum-exp over the grouped heads' scores
+    kr = np.repeat(k, H // hkv, axis=2)
+    s = np.einsum("bnhd,bmhd->bhnm", q, kr) * 0.3
+    if causal:
+        s = np.where(np.tril(np.ones((N, N), bool)), s, -np.inf)
+    np.testing.assert_allclose(lse, np.logaddexp.reduce(s, axis=3), rtol=0, atol=1e-12)
+
+
+def test_gqa_equals_attention_with_repeated_kv_heads():
+    """Grouping reduces to plain attention on K/V heads repeated per group."""
+    B, N, H, hkv, d = 2, 23, 6, 3, 8
+    q, k, v = rnd(51, (B, N, H, d)), rnd(51, (B, N, hkv, d), 1), rnd(51, (B, N, hkv, d), 2)
+    for causal in (False, True):
+        o, lse = oracle.attention_gqa(q, k, v, 0.4, causal)
+        o2, lse2 = oracle.attention(q, np.repeat(k, 2, axis=2), np.repeat(v, 2, axis=2), 0.4,
+                                    causal)
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(lse, lse2)
+
+
+def test_queries_at_the_end_equal_the_last_rows_of_full_causal_attention():
+    """Nq queries against Nk >= Nq keys, causal: they are the last Nq
+    positions, so the result equals the last Nq rows of square causal
+    attention (catches top-left alignment where the keys are longer)."""
+    B, Nk, Nq, H, d = 2, 40, 7, 2, 8
+    qf, k, v = rnd(52, (B, Nk, H, d)), rnd(52, (B, Nk, H, d), 1), rnd(52, (B, Nk, H, d), 2)
+    of, lf = oracle.attention(qf, k, v, 0.5, True)
+    o, lse = oracle.attention_gqa(qf[:, Nk - Nq:], k, v, 0.5, True)
+    np.testing.assert_array_equal(o, of[:, Nk - Nq:])
+    np.testing.assert_array_equal(lse, lf[:, :, Nk - Nq:])
+
+
+def test_queries_at_the_end_match_torch_with_explicit_mask():
+    B, Nk, Nq, H, d = 1, 11, 4, 2, 8
+    q, k, v = rnd(53, (B, Nq, H, d)), rnd(53, (B, Nk, H, d), 1), rnd(53, (B, Nk, H, d), 2)
+    o, _ = oracle.attention_gqa(q, k, v, 0.5, True)
+    mask = torch.from_numpy(np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq))
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                                           scale=0.5)
+    np.testing.assert_allclose(o, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+
+
+def test_query_with_no_allowed_key_is_empty():
+    """More queries than keys, causal: the first Nq - Nk queries see no key
+    (O = 0, lse = -inf by the stated convention)."""
+    q, k, v = rnd(54, (1, 5, 1, 4)), rnd(54, (1, 3, 1, 4), 1), rnd(54, (1, 3, 1, 4), 2)
+    o, lse = oracle.attention_gqa(q, k, v, 1.0, True)
+    assert np.all(o[0, :2] == 0) and np.all(np.isneginf(lse[0, 0, :2]))
+    assert np.isfinite(lse[0, 0, 2:]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_equals_contiguous(causal):
+    """Keys read through a shuffled page table give the contiguous result
+    (catches a wrong page / row split of the token index)."""
+    B, H, hkv, d, P = 3, 4, 2, 8, 16
+    seqlens = [37, 16, 50]
+    Nq = 5
+    npages = sum((L + P - 1) // P for L in seqlens) + 3
+    rng = np.random.default_rng(55)
+    perm = rng.permutation(npages)
+    kc, vc = rnd(55, (npages, P, hkv, d), 1), rnd(55, (npages, P, hkv, d), 2)
+    table, used = [], 0
+    for L in seqlens:
+        n = (L + P - 1) // P
+        table.append(perm[used:used + n])
+        used += n
+    q = rnd(55, (B, Nq, H, d))
+    o, lse = oracle.attention_paged(q, kc, vc, table, seqlens, 0.35, causal)
+    for b, L in enumerate(seqlens):
+        rows = np.concatenate([np.arange(P) + P * pg for pg in table[b]])[:L]
+        kb = kc.reshape(-1, hkv, d)[rows][None]
+        vb = vc.reshape(-1, hkv, d)[rows][None]
+        ob, lb = oracle.attention_gqa(q[b:b + 1], kb, vb, 0.35, causal)
+        np.testing.assert_array_equal(o[b], ob[0])
+        np.testing.assert_array_equal(lse[b], lb[0])
+
+
+def test_merge_of_key_ranges_equals_unsplit_attention():
+    """Attention over disjoint key ranges, merged, equals attention over all
+    keys (the combine step of split-key decoding), including an empty part."""
+    N, H, d = 45, 2, 8
+    q, k, v = rnd(56, (1, N, H, d)), rnd(56, (1, N, H, d), 1), rnd(56, (1, N, H, d), 2)
+    o_full, lse_full = oracle.attention_gqa(q[:, :3], k, v, 0.4, False)
+    bounds = [0, 10, 10, 31, 45]                       # the second part is empty
+    parts_o, parts_l = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b > a:
+            o_s, l_s = oracle.attention_gqa(q[:, :3], k[:, a:b], v[:, a:b], 0.4, False)
+        else:
+            o_s, l_s = np.zeros((1, 3, H, d)), np.full((1, H, 3), -np.inf)
+        parts_o.append(o_s[0].reshape(3 * H, d))
+        parts_l.append(l_s[0].T.reshape(3 * H))
+    o, lse = oracle.merge_partials(np.stack(parts_o), np.stack(parts_l))
+    np.testing.assert_allclose(o, o_full[0].reshape(3 * H, d), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_full[0].T.reshape(3 * H), rtol=0, atol=1e-13)
