@@ -9,6 +9,7 @@ built, every call raises.
     o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen)      # [T,H,d]
     q8, k8, v8, dq, dk, dv = qkv_block_quant_hadamard(q, k, v, signs)
     o, lse = attn_fwd_fp8(q8, k8, v8, dq, dk, dv)
+    o, lse = attn_fwd_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen_k)
 """
 from __future__ import annotations
 
@@ -27,8 +28,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT",
           6: "ATTN_ERR_BAD_SEQLENS", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_TOO_LARGE"}
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_fp8", "qkv_block_quant_hadamard",
-           "attn_get_status", "attn_fwd_varlen_noalloc", "attn_status_string",
-           "attn_shutdown", "attn_version")
+           "attn_get_status", "attn_fwd_varlen_noalloc", "attn_fwd_gqa", "attn_fwd_varlen_gqa",
+           "attn_fwd_paged", "attn_status_string", "attn_shutdown", "attn_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -62,11 +63,16 @@ def lib() -> ctypes.CDLL:
                                                    i, i, i, i, vp]
             L.attn_fwd_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i,
                                                   i, vp, vp]
+            L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+            L.attn_fwd_varlen_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i,
+                                              vp]
             L.attn_get_status.argtypes = [vp]
             L.attn_status_string.argtypes = [i]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_version.restype = ctypes.c_uint32
-            for nm in EXPORTS[:6]:
+            L.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
+                                         i, f, i, i, i, vp]
+            for nm in EXPORTS[:9]:
                 getattr(L, nm).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -103,18 +109,26 @@ def _need_cuda(*ts):
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
              want_lse: bool = True, stream=None):
-    """Dense attention, q/k/v [B, N, H, d] bf16 or fp16 -> (o [B,N,H,d], lse [B,H,N] fp32)."""
+    """Dense attention, q [B, N, H, d], k/v [B, N, H_kv, d] (H_kv divides H;
+    H_kv < H is grouped-query attention), bf16 or fp16
+    -> (o [B,N,H,d], lse [B,H,N] fp32)."""
     _need_cuda(q, k, v)
     B, N, H, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must have the same shape and dtype")
+    Hkv = k.shape[2]
+    if (k.shape != (B, N, Hkv, d) or v.shape != k.shape or k.dtype != q.dtype
+            or v.dtype != q.dtype):
+        raise ValueError("q [B,N,H,d] and k, v [B,N,H_kv,d] must agree in shape and dtype")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     _need_cuda(o, lse)
-    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
-                        int(bool(causal)), _dtype_code(q), _stream(stream))
+    if Hkv == H:
+        rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                            int(bool(causal)), _dtype_code(q), _stream(stream))
+    else:
+        rc = lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                scale, int(bool(causal)), _dtype_code(q), _stream(stream))
     _check(rc, "attn_fwd")
     return o, lse
 
@@ -122,20 +136,30 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
 def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
                     scale: float | None = None, out=None, lse=None, want_lse: bool = True,
                     stream=None):
-    """Packed attention, q/k/v [T, H, d], cu_seqlens int32 [nseq+1] on the device
-    -> (o [T,H,d], lse [H,T] fp32)."""
+    """Packed attention, q [T, H, d], k/v [T, H_kv, d], cu_seqlens int32
+    [nseq+1] on the device -> (o [T,H,d], lse [H,T] fp32)."""
     _need_cuda(q, k, v, cu_seqlens)
     T, H, d = q.shape
+    Hkv = k.shape[1]
     if cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError("q [T,H,d] and k, v [T,H_kv,d] must agree in shape")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None and want_lse:
         lse = torch.empty((H, T), device=q.device, dtype=torch.float32)
     _need_cuda(o, lse)
-    rc = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
-                               cu_seqlens.numel() - 1, T, int(max_seqlen), H, d, scale,
-                               int(bool(causal)), _dtype_code(q), _stream(stream))
+    if Hkv == H:
+        rc = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                   _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen),
+                                   H, d, scale, int(bool(causal)), _dtype_code(q),
+                                   _stream(stream))
+    else:
+        rc = lib().attn_fwd_varlen_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                       _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                       int(max_seqlen), H, Hkv, d, scale, int(bool(causal)),
+                                       _dtype_code(q), _stream(stream))
     _check(rc, "attn_fwd_varlen")
     return o, lse
 
@@ -157,6 +181,33 @@ def attn_fwd_varlen_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, lse=None,
                                        _dtype_code(q), _ptr(status), _stream(stream))
     _check(rc, "attn_fwd_varlen_noalloc")
     return out, lse
+
+
+def attn_fwd_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen_k: int,
+                   causal: bool = True, scale: float | None = None, num_splits: int = 0,
+                   out=None, lse=None, want_lse: bool = True, stream=None):
+    """Decoding against a paged K/V cache: q [B, Nq, H, d] (the newest Nq
+    positions), k_cache/v_cache [num_pages, page_size, H_kv, d], block_table
+    int32 [B, max_pages], seqlens_k int32 [B] (all on the device)
+    -> (o [B, Nq, H, d], lse [B, H, Nq] fp32)."""
+    _need_cuda(q, k_cache, v_cache, block_table, seqlens_k)
+    B, Nq, H, d = q.shape
+    num_pages, page_size, Hkv, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d or k_cache.dtype != q.dtype:
+        raise ValueError("k_cache, v_cache must be [num_pages, page_size, H_kv, d] of q's dtype")
+    if block_table.dtype != torch.int32 or seqlens_k.dtype != torch.int32:
+        raise TypeError("block_table and seqlens_k must be int32")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    _need_cuda(o, lse)
+    rc = lib().attn_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                              _ptr(seqlens_k), _ptr(o), _ptr(lse), B, Nq, H, Hkv, d, page_size,
+                              block_table.shape[1], num_pages, int(max_seqlen_k), scale,
+                              int(bool(causal)), _dtype_code(q), int(num_splits), _stream(stream))
+    _check(rc, "attn_fwd_paged")
+    return o, lse
 
 
 def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool = False,

@@ -43,6 +43,9 @@
 //  * the output is rescaled only when a row max grows by more than
 //    kRescaleThresh (log2 units); otherwise the stale max is kept, which is
 //    exact after the final division by l;
+//  * e4m3: the V descale of each key block is folded into P (stored as
+//    e4m3(p * w)) with w kept in [1, 8] by re-basing the output's unit,
+//    which rescales O like a grown row max;
 //  * every mbarrier wait is bounded (clock64 budget): on expiry the kernel
 //    records ATTN_ERR_TIMEOUT in the status word, drains its own copies and
 //    MMAs, frees TMEM and returns; the e4m3 pair barriers AND their warps'
@@ -62,13 +65,14 @@ struct Params {
   const int2 *tiles;        // varlen: (sequence, query-tile) in schedule order
   const int *num_entries;   // varlen: number of valid entries in `tiles`
   int B;                    // dense: batch; varlen: number of sequences
-  int H;
+  int H;                    // query (and output) heads
+  int grp;                  // query heads per K/V head (H / H_kv)
   int N;                    // dense: sequence length; varlen: max sequence length
   int T;                    // varlen: total tokens
   int num_tiles;            // dense: exact count; varlen: upper bound
   int causal;
   float scale_log2;         // scale * log2(e)
-  const float *dq, *dk, *dv;  // e4m3: per-block descales [B,H,nblk]
+  const float *dq, *dk, *dv;  // e4m3: per-block descales [B,H,nblk] (Q), [B,H_kv,nblk] (K, V)
   int nblk;
   long long wait_budget;
   int *status;
@@ -97,6 +101,12 @@ struct Cfg {
   static constexpr int NS = kRingFit >= 8 ? 8 : (kRingFit >= 4 ? 4 : 2);
   static_assert(NS >= 3, "K/V ring too small");
   static_assert((NS & (NS - 1)) == 0, "K/V ring size must be a power of two");
+  // K and V tiles alternate through the ring, so with an even ring a slot
+  // always holds K (consumed by the S issuer) or always V (the O issuer), and
+  // each full barrier has one waiter that sees its phases in order.  With an
+  // odd ring one issuer could reach a slot's next use while the other's use
+  // of it is still pending, and its parity wait would pass a phase early.
+  static_assert(NS % 2 == 0, "K/V ring size must be even");
   // MMA shapes.  Each instruction consumes 32 bytes of K per row.
   static constexpr int kKStep = 32 / kElt;             // 16 (16-bit) or 32 (e4m3)
   static constexpr int kQKSteps = kRowBytes / 32;
@@ -109,10 +119,13 @@ struct Cfg {
   static constexpr uint32_t kColO0 = 256;
   static constexpr int kPCols = BN * kElt / 4;         // 64 (16-bit P) or 32 (e4m3 P)
   // Output rescale threshold in log2 units: p may grow to 2^thresh between
-  // rescales.  16-bit P: 2^8.  e4m3 P is stored as p * (kP8Scale * dv_j /
-  // dv_max) <= 2^3.75 * 32 = 430, below the e4m3 maximum 448.
-  static constexpr float kP8Scale = 32.f;
-  static constexpr float kRescaleThresh = kFp8 ? 3.75f : 8.0f;
+  // rescales.  16-bit P: 2^8.  e4m3 P is stored as p * w with the prescale
+  // w <= kP8Scale: at most 2^5.75 * 8 = 430, below the e4m3 maximum 448.  (A
+  // larger prescale buys nothing in accuracy and a lower threshold; with
+  // outlier keys a 32-row warp then rescales O on a quarter of its key
+  // blocks instead of a twelfth.)
+  static constexpr float kP8Scale = 8.f;
+  static constexpr float kRescaleThresh = kFp8 ? 5.75f : 8.0f;
   // e4m3: P goes to shared memory (one 128 x 128-byte tile per sub-tile, the
   // 128-byte-swizzled K-major layout), so S can be overwritten as soon as the
   // softmax has read it; 16-bit P stays in TMEM over S.
@@ -131,9 +144,9 @@ struct Cfg {
   static constexpr int kWarpTMA = kSoftmaxWarps + 1;   // TMA producer
   static constexpr int kWarpPV = kSoftmaxWarps + 2;    // e4m3: second issuer (O += P V)
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 2 + (kDual ? 1 : 0));
-  // arrivals per phase on the barriers the softmax signals: one per thread
-  // (16-bit), one per warp (e4m3)
-  static constexpr int kSoftArrive = kSplit ? 8 : 128;
+  // arrivals per phase on the barriers the softmax signals: one per softmax
+  // thread of the sub-tile
+  static constexpr int kSoftArrive = 32 * kSoftmaxWarps / 2;
   // shared memory layout (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
@@ -146,11 +159,13 @@ struct Cfg {
   static constexpr int kOffRed = (kOffMisc + 64 + 15) / 16 * 16;
   static constexpr int kRedBytes = kSplit ? (1024 + 512) * 4 : 0;
   static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024 /* alignment slack */ + 1024 /* guard */;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeded");
 };
 
 struct TileInfo {
   int b;          // dense batch index / varlen sequence index
-  int h;
+  int h;          // query head
+  int hk;         // its K/V head
   int qt;         // query tile (256 rows) within the sequence
   int L;          // sequence length
   int start;      // first token of the sequence in the packed / flattened rows
@@ -187,6 +202,7 @@ __device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, 
     ti.start = p.cu_seqlens[e.x];
     ti.L = p.cu_seqlens[e.x + 1] - ti.start;
   }
+  ti.hk = ti.h / p.grp;
   const int nkv = (ti.L + 127) / 128;
   if (p.causal) {
     ti.nA = min(2 * ti.qt + 1, nkv);
@@ -303,10 +319,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int c = 0; c < C::kChunks; ++c) {
               uint8_t *dst = sKV + slot * C::kTileBytes + c * C::kChunkBytes;
               if constexpr (C::kVarlen)
-                tma_load_3d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.h,
+                tma_load_3d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk,
                             ti.start + j * 128);
               else
-                tma_load_4d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.h, j * 128, ti.b);
+                tma_load_4d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk, j * 128,
+                            ti.b);
             }
           }
         }
@@ -705,18 +722,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int row = row0 + r_in;
       float m_run = -INFINITY;                          // running max, log2 units
       float l_run = 0.f;                                // this half's running sum
-      // per-block descales of this (b, h); P is stored as p * pw with
-      // pw = kP8Scale * dv_j / dv_max, undone in the epilogue
+      // Per-block descales of this (b, h).  The V descale dv_j of key block
+      // j is folded into P: it is stored as p * w, w = kP8Scale * dv_j / R,
+      // so O accumulates in units of R / kP8Scale.  R starts at the largest
+      // dv of the (b, h); when w would leave [kP8Scale / 8, kP8Scale] (a
+      // block whose scale is far below R, or above it after such a change),
+      // R is re-based to dv_j and O rescaled with it, like the row maximum.
       const size_t dbase = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
+      const size_t kvbase = (static_cast<size_t>(ti.b) * (p.H / p.grp) + ti.hk) * p.nblk;
       const float dq_s = __ldg(p.dq + dbase + (row0 >> 7));
-      const float *dk_row = p.dk + dbase;
-      const float *dv_row = p.dv + dbase;
+      const float *dk_row = p.dk + kvbase;
+      const float *dv_row = p.dv + kvbase;
       float dvm = 0.f;
       for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
 #pragma unroll
       for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
-      const float inv_dv_max = C::kP8Scale / dvm;
-      const float pv_scale = dvm / C::kP8Scale;
+      float r_unit = C::kP8Scale / dvm;                 // kP8Scale / R
       float dk_next = __ldg(dk_row), dv_next = __ldg(dv_row);
       bool good = true;   // every wait of this warp so far succeeded
       for (int j = 0; j < nX; ++j) {
@@ -727,10 +748,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tmem_ld64(tS, sv);
         // S is in registers: the tensor core may overwrite it
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_s_free[x]);
+        mbar_arrive(&bar_s_free[x]);
         const float cs = p.scale_log2 * dq_s * dk_next;   // log2 units per raw score
-        const float pw = dv_next * inv_dv_max;
+        float pw = dv_next * r_unit;
+        float unit_f = 1.f;                                 // O rescale from re-basing R
+        // (the upper test has a little slack so that the block that sets R
+        // does not re-base through rounding; p * w stays below 448 up to
+        // w = 8.3)
+        if (pw < C::kP8Scale * 0.125f || pw > C::kP8Scale * 1.03125f) {   // uniform over (b, h)
+          unit_f = C::kP8Scale / pw;
+          r_unit = C::kP8Scale / dv_next;
+          pw = C::kP8Scale;
+        }
         if (j + 1 < nX) {
           dk_next = __ldg(dk_row + j + 1);
           dv_next = __ldg(dv_row + j + 1);
@@ -805,19 +834,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                  ex2(-lpw);
         // Rescale this half of O_X (the previous update has landed, and
         // O_X += P_X(j) V_j waits for the arrival below).
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > 0 && (unit_f != 1.f || __any_sync(0xffffffffu, resc))) {
+          const float f = alpha * unit_f;
 #pragma unroll 1
           for (int c = 0; c < C::D / 64; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             tmem_st32(tO + c * 32, o);
           }
         }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p_full[x]);
+        mbar_arrive(&bar_p_full[x]);
       }
       if (!ok) break;
       // ---------------- epilogue: O / l, lse ----------------
@@ -827,7 +856,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const float l_row = l_run + red_sum[(x * 2 + (kh ^ 1)) * 128 + r_in];
       tc_fence_after();
       const bool valid = row < ti.L;
-      const float inv_l = (l_row > 0.f) ? pv_scale / l_row : 0.f;
+      const float inv_l = (l_row > 0.f) ? 1.f / (r_unit * l_row) : 0.f;
       uint32_t *orow = nullptr;
       if (valid) {
         const size_t tok = static_cast<size_t>(ti.start) + row;
@@ -857,8 +886,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.N + row] = lse;
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_o_free[x]);
+      mbar_arrive(&bar_o_free[x]);
     }
   }
 

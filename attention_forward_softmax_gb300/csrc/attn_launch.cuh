@@ -17,18 +17,20 @@ CUtensorMapDataType tma_dtype() {
   else return CU_TENSOR_MAP_DATA_TYPE_UINT8;
 }
 
+// Tensor map of Q (heads = H) or K / V (heads = H_kv).
 template <class C>
-attn_status_t make_qkv_map(CUtensorMap *m, const void *ptr, const LaunchArgs &a) {
+attn_status_t make_qkv_map(CUtensorMap *m, const void *ptr, const LaunchArgs &a, int heads) {
   const cuuint64_t e = C::kElt;
   if constexpr (C::kVarlen) {
-    const cuuint64_t dims[3] = {(cuuint64_t)C::D, (cuuint64_t)a.H, (cuuint64_t)a.T};
-    const cuuint64_t strides[2] = {C::D * e, (cuuint64_t)a.H * C::D * e};
+    const cuuint64_t dims[3] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)a.T};
+    const cuuint64_t strides[2] = {C::D * e, (cuuint64_t)heads * C::D * e};
     const cuuint32_t box[3] = {(cuuint32_t)C::kChunkElems, 1, 128};
     return encode_tiled(m, tma_dtype<C>(), 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    const cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)a.H, (cuuint64_t)a.N, (cuuint64_t)a.B};
-    const cuuint64_t strides[3] = {C::D * e, (cuuint64_t)a.H * C::D * e,
-                                   (cuuint64_t)a.N * a.H * C::D * e};
+    const cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)a.N,
+                                (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {C::D * e, (cuuint64_t)heads * C::D * e,
+                                   (cuuint64_t)a.N * heads * C::D * e};
     const cuuint32_t box[4] = {(cuuint32_t)C::kChunkElems, 1, 128, 1};
     return encode_tiled(m, tma_dtype<C>(), 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
@@ -38,9 +40,9 @@ template <class C>
 attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   attn_status_t st;
-  if ((st = make_qkv_map<C>(&mq, a.q, a)) != ATTN_OK) return st;
-  if ((st = make_qkv_map<C>(&mk, a.k, a)) != ATTN_OK) return st;
-  if ((st = make_qkv_map<C>(&mv, a.v, a)) != ATTN_OK) return st;
+  if ((st = make_qkv_map<C>(&mq, a.q, a, a.H)) != ATTN_OK) return st;
+  if ((st = make_qkv_map<C>(&mk, a.k, a, a.Hkv)) != ATTN_OK) return st;
+  if ((st = make_qkv_map<C>(&mv, a.v, a, a.Hkv)) != ATTN_OK) return st;
   Params p{};
   p.o = a.o;
   p.lse = a.lse;
@@ -49,6 +51,7 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   p.num_entries = a.num_entries;
   p.B = a.B;
   p.H = a.H;
+  p.grp = a.H / a.Hkv;
   p.N = a.N;
   p.T = a.T;
   p.num_tiles = a.num_tiles;

@@ -1,0 +1,464 @@
+// decode.cu -- attention of a few new queries per sequence against a paged
+// K/V cache, split over key ranges, and the merge of the partial results
+// (the inference variants the pages point to: "Paged Attention" among the
+// additions of the HippoAttention case study, streamhpc.com, "Our
+// approach"; "optimizing for LLM inference", FlashAttention-3 summary,
+// arxivlens, Limitations).
+//
+// What it computes is exact attention (the "Fused attention kernel" concept
+// card, Overview): for each query row, softmax(scale * q K^T) V and the
+// natural-log lse over the allowed keys of its sequence.  The keys of
+// sequence b are its first seqlens_k[b] cache positions; position t lives in
+// row t % page_size of page block_table[b][t / page_size].  The Nq queries
+// are the last Nq positions (causal: query i sees keys j <= L - Nq + i).
+// Query head h uses K/V head h / (H / H_kv).
+//
+// Design.  Decoding is bound by HBM: each key brings 4 d bytes of K and V
+// and meets only the R = (H / H_kv) * Nq query rows of its K/V head.  So one
+// CTA takes one (sequence, K/V head, key range) and streams that range once:
+//  * 128-key tiles of K and V are gathered row by row through the page table
+//    with 16-byte cp.async copies into XOR-swizzled shared-memory tiles, two
+//    stages deep, so the next tile's rows are in flight while this one is
+//    used;
+//  * the R <= 16 query rows are one 16-row MMA tile; each of the four warps
+//    takes 32 keys of a tile and runs the running-softmax loop on them with
+//    warp-level bf16/fp16 MMAs (m16n8k16: S = Q K^T, then O += P V with P
+//    taken from the score registers).  The contractions are tiny -- 16 rows
+//    -- so the tensor pipe is nowhere near the limit; the bytes are;
+//  * the four warps' (max, sum, O) are merged through shared memory; with one
+//    split the CTA writes O and lse, otherwise fp32 partials that
+//    merge_kernel combines: lse = log sum_s exp(lse_s), O = sum_s
+//    exp(lse_s - lse) O_s.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr int kTileKeys = 128;     // keys per tile (32 per warp)
+constexpr int kRows = 16;          // query rows per CTA (one MMA tile)
+
+struct DecodeArgs {
+  const void *q;                   // [B, Nq, H, d]
+  const void *k, *v;               // [num_pages, page_size, H_kv, d]
+  const int *block_table;          // [B, max_pages]
+  const int *seqlens_k;            // [B]
+  void *o;                         // [B, Nq, H, d]
+  float *lse;                      // [B, H, Nq] or null
+  float *ws_o;                     // [splits, B, H, Nq, d] fp32 partials (splits > 1)
+  float *ws_lse;                   // [splits, B, H, Nq]
+  int B, Nq, H, Hkv, page_size, max_pages, num_pages, splits;
+  float scale_log2;
+  int causal;
+};
+
+template <int D>
+struct DecSmem {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kTileBytes = kTileKeys * kRowBytes;     // one K or V tile
+  static constexpr int kOffQ = 0;                              // 16 rows
+  static constexpr int kOffKV = kRows * kRowBytes;             // [stage][K, V]
+  static constexpr int kBytes = kOffKV + 2 * 2 * kTileBytes;
+  // after the key loop the K/V area holds the warps' partial results
+  static_assert(4 * kRows * (D + 2) * 4 <= 2 * 2 * kTileBytes, "merge area too small");
+};
+
+// 16-byte chunk c of row r of a swizzled tile (rows of D 16-bit values):
+// chunk c is stored at c ^ (r mod 8), so 8 rows read at one chunk hit 8
+// different bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return r * (D * 2) + ((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D(16x8, f32) += A(16x16) * B(16x8), 16-bit operands
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (BF16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_kernel(const DecodeArgs a) {
+  using L = DecSmem<D>;
+  constexpr int kChunks = D / 8;           // 16-byte chunks per row
+  constexpr int kNT = D / 8;               // 8-column output tiles
+  extern __shared__ __align__(128) uint8_t dsm[];
+  const uint32_t sbase = smem_addr(dsm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int g = a.H / a.Hkv;               // query heads per K/V head
+  const int R = g * a.Nq;                  // query rows of this K/V head (<= 16)
+  const int Lk = __ldg(a.seqlens_k + b);
+  // key range of this split: whole tiles, the last split takes the rest
+  const int ntiles = (Lk + kTileKeys - 1) / kTileKeys;
+  const int per = (ntiles + a.splits - 1) / a.splits;
+  const int t0 = split * per, t1 = min(ntiles, t0 + per);
+  const int k1 = min(Lk, t1 * kTileKeys);
+  const size_t row_stride = static_cast<size_t>(a.Hkv) * D;   // elements between cache rows
+  const uint16_t *kc = static_cast<const uint16_t *>(a.k);
+  const uint16_t *vc = static_cast<const uint16_t *>(a.v);
+
+  // query rows r = qi * g + gh (query qi, head hk * g + gh) -> shared memory
+  {
+    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+    for (int id = threadIdx.x; id < kRows * kChunks; id += kDecThreads) {
+      const int r = id / kChunks, c = id % kChunks;
+      const int qi = r / g, gh = r % g;
+      const uint16_t *src = qg + ((static_cast<size_t>(b) * a.Nq + (r < R ? qi : 0)) * a.H +
+                                  hk * g + (r < R ? gh : 0)) * D + c * 8;
+      cp_async16(sbase + L::kOffQ + swz<D>(r, c), src, r < R ? 16 : 0);
+    }
+  }
+  // gather one tile of K and V through the page table
+  auto load_tile = [&](int tile, int stage) {
+    const uint32_t kdst = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
+    const uint32_t vdst = kdst + L::kTileBytes;
+    for (int id = threadIdx.x; id < kTileKeys * kChunks; id += kDecThreads) {
+      const int r = id / kChunks, c = id % kChunks;
+      const int t = tile * kTileKeys + r;
+      const bool ok = t < k1;
+      const int page = ok ? __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages +
+                                  t / a.page_size)
+                          : 0;
+      const size_t row = ok ? static_cast<size_t>(page) * a.page_size + t % a.page_size : 0;
+      const size_t off = row * row_stride + static_cast<size_t>(hk) * D + c * 8;
+      cp_async16(kdst + swz<D>(r, c), kc + off, ok ? 16 : 0);
+      cp_async16(vdst + swz<D>(r, c), vc + off, ok ? 16 : 0);
+    }
+  };
+
+  // per-warp running state for the 16 rows: lane holds rows ra = lane/4 and
+  // rb = ra + 8 of every accumulator tile
+  const int ra = lane >> 2, rb = ra + 8, tq = lane & 3;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float o[kNT][4];
+#pragma unroll
+  for (int n = 0; n < kNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  // last allowed key of each row (causal: queries are the last Nq positions)
+  const int lim_a = a.causal ? Lk - a.Nq + ra / g : Lk - 1;
+  const int lim_b = a.causal ? Lk - a.Nq + rb / g : Lk - 1;
+
+  if (t0 < t1) load_tile(t0, 0);
+  cp_async_commit();
+  uint32_t qf[D / 16][4];                  // Q fragments, loaded once
+  for (int tile = t0; tile < t1; ++tile) {
+    const int stage = (tile - t0) & 1;
+    if (tile + 1 < t1) load_tile(tile + 1, stage ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (tile == t0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        ldsm_x4(sbase + L::kOffQ + swz<D>(lane & 15, 2 * ks + (lane >> 4)), qf[ks]);
+    }
+    const uint32_t kt = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
+    const uint32_t vt = kt + L::kTileBytes;
+    const int kw = warp * 32;              // this warp's keys within the tile
+    // S = Q K^T for 32 keys: four 8-key tiles
+    float s[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {     // two 8-key tiles per ldmatrix
+        uint32_t kb[4];
+        const int key = kw + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        ldsm_x4(kt + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), kb);
+        mma16816<BF16>(s[2 * np], qf[ks], kb[0], kb[1]);
+        mma16816<BF16>(s[2 * np + 1], qf[ks], kb[2], kb[3]);
+      }
+    // mask, then the running softmax in log2 units
+    const int kbase = tile * kTileKeys + kw;
+    float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kbase + n * 8 + 2 * tq + e;
+        s[n][e] = (key <= lim_a && key < k1) ? s[n][e] * a.scale_log2 : -INFINITY;
+        s[n][2 + e] = (key <= lim_b && key < k1) ? s[n][2 + e] * a.scale_log2 : -INFINITY;
+        mx_a = fmaxf(mx_a, s[n][e]);
+        mx_b = fmaxf(mx_b, s[n][2 + e]);
+      }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, m));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, m));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    const float al_a = mn_a == -INFINITY ? 1.f : ex2(m_a - mn_a);
+    const float al_b = mn_b == -INFINITY ? 1.f : ex2(m_b - mn_b);
+    const float mu_a = mn_a == -INFINITY ? 0.f : mn_a, mu_b = mn_b == -INFINITY ? 0.f : mn_b;
+    m_a = mn_a;
+    m_b = mn_b;
+    float ps_a = 0.f, ps_b = 0.f;
+    uint32_t pf[2][4];                     // P as A fragments of two 16-key steps
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const float p0 = ex2(s[n][0] - mu_a), p1 = ex2(s[n][1] - mu_a);
+      const float p2 = ex2(s[n][2] - mu_b), p3 = ex2(s[n][3] - mu_b);
+      ps_a += p0 + p1;
+      ps_b += p2 + p3;
+      const uint32_t pa = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+      const uint32_t pb = BF16 ? pack_bf16(p2, p3) : pack_f16(p2, p3);
+      pf[n >> 1][(n & 1) * 2 + 0] = pa;   // rows ra: keys 2t.. (+8 for the odd tile)
+      pf[n >> 1][(n & 1) * 2 + 1] = pb;   // rows rb
+    }
+    l_a = l_a * al_a + ps_a;
+    l_b = l_b * al_b + ps_b;
+#pragma unroll
+    for (int n = 0; n < kNT; ++n) {
+      o[n][0] *= al_a;
+      o[n][1] *= al_a;
+      o[n][2] *= al_b;
+      o[n][3] *= al_b;
+    }
+    // O += P V: two 16-key steps, d/8 column tiles (two per ldmatrix)
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+      for (int np = 0; np < kNT / 2; ++np) {
+        uint32_t vb[4];
+        const int key = kw + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        ldsm_x4_t(vt + swz<D>(key, 2 * np + (lane >> 4)), vb);
+        mma16816<BF16>(o[2 * np], pf[ks], vb[0], vb[1]);
+        mma16816<BF16>(o[2 * np + 1], pf[ks], vb[2], vb[3]);
+      }
+    __syncthreads();                       // this stage may be refilled next
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // merge the four warps' partial results through shared memory
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  float *mrg = reinterpret_cast<float *>(dsm + L::kOffKV);   // [warp][row][D + 2]
+  float *mw = mrg + warp * kRows * (D + 2);
+#pragma unroll
+  for (int n = 0; n < kNT; ++n) {
+    mw[ra * (D + 2) + n * 8 + 2 * tq] = o[n][0];
+    mw[ra * (D + 2) + n * 8 + 2 * tq + 1] = o[n][1];
+    mw[rb * (D + 2) + n * 8 + 2 * tq] = o[n][2];
+    mw[rb * (D + 2) + n * 8 + 2 * tq + 1] = o[n][3];
+  }
+  if (tq == 0) {
+    mw[ra * (D + 2) + D] = m_a;
+    mw[ra * (D + 2) + D + 1] = l_a;
+    mw[rb * (D + 2) + D] = m_b;
+    mw[rb * (D + 2) + D + 1] = l_b;
+  }
+  __syncthreads();
+  // thread layout for the merge: 8 threads per row, D/8 columns each
+  const int r = threadIdx.x >> 3, cg = threadIdx.x & 7;
+  if (r < R) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mrg[(w * kRows + r) * (D + 2) + D]);
+    float wt[4], lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw_ = mrg[(w * kRows + r) * (D + 2) + D];
+      wt[w] = mx == -INFINITY ? 0.f : ex2(mw_ - mx);
+      lsum += wt[w] * mrg[(w * kRows + r) * (D + 2) + D + 1];
+    }
+    const int qi = r / g, h = hk * g + r % g;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float lse_r = lsum > 0.f ? (mx + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+    const size_t orow = (static_cast<size_t>(b) * a.Nq + qi) * a.H + h;   // token-major row
+    const size_t prow = (static_cast<size_t>(b) * a.H + h) * a.Nq + qi;   // [B, H, Nq] row
+    if (a.splits == 1) {
+      uint16_t *og = static_cast<uint16_t *>(a.o) + orow * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; c += 2) {
+        const int col = cg * (D / 8) + c;
+        float x[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) acc += wt[w] * mrg[(w * kRows + r) * (D + 2) + col + e];
+          x[e] = acc * inv;
+        }
+        *reinterpret_cast<uint32_t *>(og + col) = BF16 ? pack_bf16(x[0], x[1])
+                                                        : pack_f16(x[0], x[1]);
+      }
+      if (cg == 0 && a.lse != nullptr) a.lse[prow] = lse_r;
+    } else {
+      const size_t part = static_cast<size_t>(split) * a.B * a.H * a.Nq + prow;
+      float *wo = a.ws_o + part * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const int col = cg * (D / 8) + c;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc += wt[w] * mrg[(w * kRows + r) * (D + 2) + col];
+        wo[col] = acc * inv;
+      }
+      if (cg == 0) a.ws_lse[part] = lse_r;
+    }
+  }
+}
+
+// Combine the splits' partial (O, lse) of each (b, h, query) row: one warp
+// per row.  A split that saw no key has lse = -inf and weight 0.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int rows = a.B * a.H * a.Nq;
+  if (row >= rows) return;
+  const size_t stride = static_cast<size_t>(rows);
+  float mx = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) mx = fmaxf(mx, a.ws_lse[s * stride + row]);
+  float acc[D / 32] = {}, z = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < a.splits; ++s) {
+      const float w = __expf(a.ws_lse[s * stride + row] - mx);
+      z += w;
+      const float *po = a.ws_o + (s * stride + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) acc[c] += w * po[lane + 32 * c];
+    }
+  }
+  // row = (b * H + h) * Nq + qi  ->  token-major output row (b, qi, h)
+  const int qi = row % a.Nq, h = (row / a.Nq) % a.H, b = row / (a.Nq * a.H);
+  uint16_t *og = static_cast<uint16_t *>(a.o) + ((static_cast<size_t>(b) * a.Nq + qi) * a.H + h) * D;
+  const float inv = z > 0.f ? 1.f / z : 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    const float x = acc[c] * inv;
+    og[lane + 32 * c] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                             : __half_as_ushort(__float2half_rn(x));
+  }
+  if (lane == 0 && a.lse != nullptr) a.lse[row] = z > 0.f ? mx + logf(z) : -INFINITY;
+}
+
+template <int D, bool BF16>
+attn_status_t launch_decode(DecodeArgs &a, int num_sms, cudaStream_t s) {
+  using L = DecSmem<D>;
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t err[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::call_once(once[dev], [dev] {
+    err[dev] = cudaFuncSetAttribute(decode_kernel<D, BF16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  });
+  if (err[dev] != cudaSuccess) return ATTN_ERR_LAUNCH;
+  (void)num_sms;
+  decode_kernel<D, BF16><<<dim3(a.splits, a.Hkv, a.B), kDecThreads, L::kBytes, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (a.splits > 1) {
+    const int rows = a.B * a.H * a.Nq;
+    merge_kernel<D, BF16><<<(rows + 3) / 4, 128, 0, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" attn_status_t attn_fwd_paged(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *block_table, const int32_t *seqlens_k,
+                                        void *o, float *lse, int B, int Nq, int H, int H_kv,
+                                        int d, int page_size, int max_pages, int num_pages,
+                                        int max_seqlen_k, float scale, int causal,
+                                        attn_dtype_t dtype, int num_splits, void *stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !seqlens_k || !o) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Nq < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || page_size < 1 || max_pages < 1 ||
+      num_pages < 1 || max_seqlen_k < 1 || num_splits < 0 || !std::isfinite(scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if ((H / H_kv) * Nq > kRows) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return ATTN_ERR_MISALIGNED;
+  if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  if (static_cast<long long>(max_pages) * page_size < max_seqlen_k) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * page_size * H_kv * d > (1LL << 40) ||
+      static_cast<long long>(B) * max_pages > (1LL << 31))
+    return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  attn_status_t st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  // splits: enough CTAs to cover the SMs twice, at least one 128-key tile each
+  const int tiles = (max_seqlen_k + kTileKeys - 1) / kTileKeys;
+  int splits = num_splits;
+  if (splits == 0) {
+    const long long ctas = static_cast<long long>(B) * H_kv;
+    splits = static_cast<int>((2LL * ds->num_sms + ctas - 1) / ctas);
+  }
+  splits = std::max(1, std::min(splits, std::min(tiles, 256)));
+  DecodeArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.block_table = block_table; a.seqlens_k = seqlens_k;
+  a.o = o; a.lse = lse;
+  a.B = B; a.Nq = Nq; a.H = H; a.Hkv = H_kv; a.page_size = page_size; a.max_pages = max_pages;
+  a.num_pages = num_pages; a.splits = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal ? 1 : 0;
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(B) * H * Nq;
+    if ((st = ensure_split_workspace(ds, rows * splits * (d + 1) * sizeof(float))) != ATTN_OK)
+      return st;
+    a.ws_o = ds->split_ws;
+    a.ws_lse = ds->split_ws + rows * splits * d;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return dtype == ATTN_BF16 ? launch_decode<128, true>(a, ds->num_sms, s)
+                              : launch_decode<128, false>(a, ds->num_sms, s);
+  return dtype == ATTN_BF16 ? launch_decode<64, true>(a, ds->num_sms, s)
+                            : launch_decode<64, false>(a, ds->num_sms, s);
+}

@@ -17,6 +17,7 @@ struct LaunchArgs {
   void *o;
   float *lse;
   int B, H, N, d, T;
+  int Hkv;                   // K/V heads (H_kv divides H)
   float scale;
   int causal;
   const int *cu_seqlens;     // varlen
@@ -47,9 +48,14 @@ struct DeviceState {
   float *scratch_amax = nullptr;  // per-tensor quantisation: 3 floats
   int2 *tiles = nullptr;        // varlen tile list
   size_t tiles_cap = 0;
+  float *split_ws = nullptr;    // paged decoding: per-split partial O and lse
+  size_t split_ws_bytes = 0;
   int num_sms = 0;
 };
 attn_status_t device_state(DeviceState **out);
+// Grows the split-key workspace to at least `bytes` (waits for queued work
+// before freeing a smaller one).
+attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes);
 
 // Launches the varlen tile-list builder (one CTA) on `s`.
 cudaError_t launch_varlen_schedule(const int *cu_seqlens, int nseq, int total_tokens,

@@ -103,7 +103,7 @@ extern "C" attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, c
 
   LaunchArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = nseq; a.H = H; a.N = max_seqlen; a.d = d; a.T = total_tokens;
+  a.B = nseq; a.H = H; a.Hkv = H; a.N = max_seqlen; a.d = d; a.T = total_tokens;
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.cu_seqlens = cu_seqlens; a.tiles = tiles; a.num_entries = num_entries;
   a.num_tiles = static_cast<int>(entries * H);

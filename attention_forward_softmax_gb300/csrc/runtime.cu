@@ -68,6 +68,25 @@ attn_status_t ensure_tiles(DeviceState *ds, size_t entries) {
   return ATTN_OK;
 }
 
+attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (ds->split_ws_bytes >= bytes) return ATTN_OK;
+  size_t cap = ds->split_ws_bytes ? ds->split_ws_bytes : (1u << 20);
+  while (cap < bytes) cap *= 2;
+  if (ds->split_ws) {
+    // The old workspace may still be used by queued work: wait before freeing.
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaFree(ds->split_ws);
+    ds->split_ws = nullptr;
+    ds->split_ws_bytes = 0;
+  }
+  void *p = nullptr;
+  if (cudaMalloc(&p, cap) != cudaSuccess) return ATTN_ERR_CUDA;
+  ds->split_ws = static_cast<float *>(p);
+  ds->split_ws_bytes = cap;
+  return ATTN_OK;
+}
+
 attn_status_t encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr,
                            const cuuint64_t *dims, const cuuint64_t *strides,
                            const cuuint32_t *box, CUtensorMapSwizzle swizzle) {
@@ -179,12 +198,12 @@ using namespace attn;
 
 extern "C" {
 
-attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                       int H, int N, int d, float scale, int causal, attn_dtype_t dtype,
-                       void *stream) {
+attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int H_kv, int N, int d, float scale, int causal,
+                           attn_dtype_t dtype, void *stream) {
   attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
   if (st != ATTN_OK) return st;
-  if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   const long long tokens = static_cast<long long>(B) * N;
   const long long tiles = static_cast<long long>(B) * H * ((N + 255) / 256);
@@ -193,7 +212,8 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
   if ((st = device_state(&ds)) != ATTN_OK) return st;
   LaunchArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = B; a.H = H; a.N = N; a.d = d; a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
+  a.B = B; a.H = H; a.Hkv = H_kv; a.N = N; a.d = d;
+  a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.num_tiles = static_cast<int>(tiles);
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
@@ -201,13 +221,20 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
   return dtype == ATTN_BF16 ? launch_attn_bf16(a, false, s) : launch_attn_f16(a, false, s);
 }
 
-attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
-                              const int32_t *cu_seqlens, int nseq, int total_tokens,
-                              int max_seqlen, int H, int d, float scale, int causal,
-                              attn_dtype_t dtype, void *stream) {
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int H, int N, int d, float scale, int causal, attn_dtype_t dtype,
+                       void *stream) {
+  return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, dtype, stream);
+}
+
+attn_status_t attn_fwd_varlen_gqa(const void *q, const void *k, const void *v, void *o,
+                                  float *lse, const int32_t *cu_seqlens, int nseq,
+                                  int total_tokens, int max_seqlen, int H, int H_kv, int d,
+                                  float scale, int causal, attn_dtype_t dtype, void *stream) {
   attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
   if (st != ATTN_OK) return st;
   if (!cu_seqlens || nseq < 1 || total_tokens < 1 || max_seqlen < 1) return ATTN_ERR_INVALID_ARG;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return ATTN_ERR_MISALIGNED;
   const long long entries = static_cast<long long>(total_tokens) / 256 + nseq;
@@ -224,12 +251,20 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   LaunchArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = nseq; a.H = H; a.N = max_seqlen; a.d = d; a.T = total_tokens;
+  a.B = nseq; a.H = H; a.Hkv = H_kv; a.N = max_seqlen; a.d = d; a.T = total_tokens;
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.cu_seqlens = cu_seqlens; a.tiles = ds->tiles; a.num_entries = ds->num_entries;
   a.num_tiles = static_cast<int>(entries * H);
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
   return dtype == ATTN_BF16 ? launch_attn_bf16(a, true, s) : launch_attn_f16(a, true, s);
+}
+
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int nseq, int total_tokens,
+                              int max_seqlen, int H, int d, float scale, int causal,
+                              attn_dtype_t dtype, void *stream) {
+  return attn_fwd_varlen_gqa(q, k, v, o, lse, cu_seqlens, nseq, total_tokens, max_seqlen, H, H,
+                             d, scale, causal, dtype, stream);
 }
 
 attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *descale_q,
@@ -246,7 +281,8 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const
   if ((st = device_state(&ds)) != ATTN_OK) return st;
   LaunchArgs a{};
   a.q = q8; a.k = k8; a.v = v8; a.o = o; a.lse = lse;
-  a.B = B; a.H = H; a.N = N; a.d = d; a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
+  a.B = B; a.H = H; a.Hkv = H; a.N = N; a.d = d;
+  a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.num_tiles = static_cast<int>(tiles);
   a.dq = descale_q; a.dk = descale_k; a.dv = descale_v;
@@ -287,10 +323,11 @@ void attn_shutdown(void) {
   cudaGetDevice(&cur);
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState &ds = g_dev[d];
-    if (ds.status == nullptr && ds.tiles == nullptr) continue;
+    if (ds.status == nullptr && ds.tiles == nullptr && ds.split_ws == nullptr) continue;
     if (cudaSetDevice(d) != cudaSuccess) continue;
     cudaDeviceSynchronize();
     if (ds.tiles) cudaFree(ds.tiles);
+    if (ds.split_ws) cudaFree(ds.split_ws);
     if (ds.status) cudaFree(ds.status);
     ds = DeviceState{};
   }

@@ -57,6 +57,10 @@ def get_workload(name: str):
         return W.FP8
     if name == "varlen":
         return W.varlen_causal()
+    if name == "gqa":
+        return W.gqa_causal()
+    if name == "paged":
+        return W.paged_decode()
     if name.startswith("causal"):
         # causal:N:H:d
         _, N, H, d = name.split(":")
@@ -156,6 +160,34 @@ def build_step(w, dev):
 
     import attention_forward_softmax_gb300 as agb
     from datagen.workloads import make_inputs
+
+    from datagen.workloads import PagedWorkload, make_paged_inputs
+    if isinstance(w, PagedWorkload):
+        x = make_paged_inputs(w)
+        q = x["q"].to(dev)
+        kc, vc = x["k_cache"].to(dev), x["v_cache"].to(dev)
+        table = torch.from_numpy(x["block_table"]).to(dev)
+        seql = torch.from_numpy(x["seqlens"]).to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Nq), device=dev, dtype=torch.float32)
+
+        def step():
+            agb.attn_fwd_paged(q, kc, vc, table, seql, max(w.lengths), causal=w.causal, out=o,
+                               lse=lse)
+        # the cache is state that stays in HBM; a decoding step brings the new
+        # queries in and takes O and lse out
+        hq = x["q"].pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e():
+            q.copy_(hq, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        h2d = hq.numel() * hq.element_size()
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        return step, 2, e2e, h2d, d2h, w.flops(), step, None, (q, kc, vc, o)
 
     x = make_inputs(w)
     q, k, v = (x[n].to(dev) for n in "qkv")
@@ -339,6 +371,8 @@ def run_gpu(args):
     peaks, peak_kind = load_peaks()
     dtype = "e4m3" if w.dtype == "fp8" else w.dtype
     attn_ms = per_launch_ms(attn_only, max(10, min(args.steps, 50)), stream)
+    from datagen.workloads import PagedWorkload
+    paged = isinstance(w, PagedWorkload)
     if dtype == "e4m3":
         peak = peaks["bf16_tflops"] * 2.0          # fp8 dense = 2x bf16 (nominal ratio)
         peak_note = f"{peak_kind} bf16 burst x 2 (nominal fp8:bf16 ratio)"
@@ -352,6 +386,14 @@ def run_gpu(args):
             "peak_source": peak_note, "kernel_ms": round(attn_ms, 4),
             "algorithmic_flops_per_launch": flops,
             "frac_of_nominal_dense": round(achieved / NOMINAL_DENSE_TFLOPS[dtype], 4)}
+    if paged:
+        # decoding reads every cached K and V row once: HBM-bound (the split
+        # merge is included in the launch time)
+        gbs = w.bytes() / (attn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} HBM copy bandwidth", "kernel_ms": round(attn_ms, 4),
+                "algorithmic_bytes_per_launch": w.bytes()}
     # secondary roof: the exponential unit.  One exponential per (query,
     # allowed key) pair = flops / (4 d); the unit evaluates 32 per clock per SM
     # (ex2.approx.f32 or f16x2 pairs alike, measured on GB300), here at the
@@ -361,7 +403,7 @@ def run_gpu(args):
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     exps = flops / (4.0 * w.d)
     mufu_peak = 32.0 * n_sm * sm_mhz * 1e6
-    roof["secondary"] = {"bound": "mufu", "achieved": round(exps / (attn_ms / 1e3) / 1e12, 3),
+    roof["secondary"] = None if paged else {"bound": "mufu", "achieved": round(exps / (attn_ms / 1e3) / 1e12, 3),
                          "peak": round(mufu_peak / 1e12, 3), "unit": "Texp/s",
                          "frac": round(exps / (attn_ms / 1e3) / mufu_peak, 4),
                          "peak_source": f"32 exp2 per clock per SM x {n_sm} SMs x "
@@ -390,7 +432,28 @@ def run_gpu(args):
     e2e_steps = max(5, args.steps // 10)
 
     result = None
-    if rank == 0:
+    if rank == 0 and paged:
+        # decoding: whole-job bytes per second (every replica reads its cache)
+        result = {
+            "metric": "paged decode GB/s (cached K and V rows once, plus Q and O)",
+            "value": round(world * w.bytes() * args.steps / t / 1e9, 1), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded N(0,1) cache, shuffled pages)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "d": w.d,
+                       "Nq": w.Nq, "page_size": w.page_size, "causal": w.causal,
+                       "l2": "cache larger than L2 (no flush)" if w.bytes() > 126e6
+                       else "cache smaller than L2 (warm)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": None,
+            "e2e": {"value": round(world * w.bytes() * e2e_steps / te / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(te / e2e_steps * 1e3, 4)},
+            "gpu_launches": launches * args.steps, "clocks": cs.summary(),
+            "tflops": round(world * flops * args.steps / t / 1e12, 2),
+        }
+    elif rank == 0:
         value = job_tflops(world, flops, args.steps, t)
         cpu = None if args.no_cpu_baseline else cpu_baseline(w, budget_s=args.cpu_seconds)
         result = {
@@ -404,6 +467,7 @@ def run_gpu(args):
             (", 0.1% N(0,100) outliers" if w.outliers else "") + ")",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "varlen": w.varlen,
+                       **({"H_kv": w.Hkv} if w.Hkv else {}),
                        "l2": "inputs larger than L2 (no flush)"
                        if 3 * bufs[0].numel() * bufs[0].element_size() > 126e6
                        else "inputs smaller than L2 (cache warm)",
@@ -439,7 +503,7 @@ def oracle_sample(w, nrows: int, seed: int = 7):
     x = make_inputs(w)
     q, k, v = (x[n].to(torch.float64).numpy() for n in "qkv")   # exact up-conversion, once
     if not w.varlen:
-        q, k, v = (t.reshape(w.B * w.N, w.H, w.d) for t in (q, k, v))
+        q, k, v = (t.reshape(w.B * w.N, t.shape[2], w.d) for t in (q, k, v))
     rng = np.random.default_rng(seed)
     tok = rng.integers(0, w.tokens, size=nrows)
     head = rng.integers(0, w.H, size=nrows).astype(np.int32)
@@ -480,8 +544,9 @@ def cpu_baseline(w, budget_s: float = 15.0, threads=None):
     import oracle
     threads = threads or oracle.default_threads()
     q, k, v, cu, tok, head = oracle_sample(w, 1 << 16)
-    n, dt = calibrate(lambda m: oracle.attention_rows(q, k, v, cu, w.scale, w.causal, tok[:m],
-                                                      head[:m], threads), budget_s, len(tok))
+    n, dt = calibrate(lambda m: oracle.attention_rows_gqa(q, k, v, cu, cu, w.scale, w.causal,
+                                                          tok[:m], head[:m], threads),
+                      budget_s, len(tok))
     flops = row_flops(w, cu, tok[:n])
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
@@ -500,14 +565,15 @@ def run_reference(args):
     # size one step so that warmup + steps stay within a few minutes
     per_step_budget = args.ref_step_seconds or max(1.0, min(20.0,
                                                             150.0 / max(1, args.steps + args.warmup)))
-    n, _ = calibrate(lambda m: oracle.attention_rows(q, k, v, cu, w.scale, w.causal, tok[:m],
-                                                     head[:m], threads), per_step_budget, len(tok))
+    n, _ = calibrate(lambda m: oracle.attention_rows_gqa(q, k, v, cu, cu, w.scale, w.causal,
+                                                         tok[:m], head[:m], threads),
+                     per_step_budget, len(tok))
     for _ in range(max(0, args.warmup - 1)):
-        oracle.attention_rows(q, k, v, cu, w.scale, w.causal, tok[:n], head[:n], threads)
+        oracle.attention_rows_gqa(q, k, v, cu, cu, w.scale, w.causal, tok[:n], head[:n], threads)
     times = []
     for s in range(args.steps):
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, cu, w.scale, w.causal, tok[:n], head[:n], threads)
+        oracle.attention_rows_gqa(q, k, v, cu, cu, w.scale, w.causal, tok[:n], head[:n], threads)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     flops = row_flops(w, cu, tok[:n])
@@ -547,7 +613,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="dense",
-                    help="dense | tiny | fp8 | varlen | causal:N:H:d")
+                    help="dense | tiny | fp8 | varlen | gqa | paged | causal:N:H:d")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true",

@@ -34,6 +34,7 @@ class Workload:
     seed: int
     lengths: Optional[List[int]] = None   # varlen only
     outliers: bool = False
+    Hkv: Optional[int] = None             # K/V heads when fewer than H (grouped)
 
     @property
     def varlen(self) -> bool:
@@ -64,17 +65,18 @@ class Workload:
         return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
 
 
-def _shape(w: Workload):
-    return (w.tokens, w.H, w.d) if w.varlen else (w.B, w.N, w.H, w.d)
+def _shape(w: Workload, heads=None):
+    h = w.H if heads is None else heads
+    return (w.tokens, h, w.d) if w.varlen else (w.B, w.N, h, w.d)
 
 
 def make_inputs(w: Workload) -> dict:
     """Seeded Q, K, V (CPU tensors, bf16 or fp16; layout [B,N,H,d] dense or
     [T,H,d] packed), plus cu_seqlens (int32) and, for fp8, the sign vector."""
-    shape = _shape(w)
     conv = to_fp16 if w.dtype == "fp16" else to_bf16
     out = {}
     for s, nm in enumerate("qkv"):
+        shape = _shape(w, None if nm == "q" else w.Hkv)
         if w.outliers:
             x = outlier_normal(w.seed, s, shape)
         else:
@@ -110,3 +112,64 @@ def varlen_causal() -> Workload:
     lens = varlen_lengths(1005, 32, 64, 4096)
     return Workload("bf16 causal varlen 32 seqs L~U[64,4096] H=32 d=128", "bf16",
                     32, 32, max(lens), 128, True, 1005, lengths=lens)
+
+
+def gqa_causal() -> Workload:
+    """Grouped K/V heads (8 query heads per K/V head), causal prefill."""
+    return Workload("bf16 causal GQA B=4 H=32 H_kv=8 N=8192 d=128", "bf16", 4, 32, 8192, 128,
+                    True, 1006, Hkv=8)
+
+
+@dataclass
+class PagedWorkload:
+    """Decoding against a paged K/V cache: each sequence has `lengths[b]`
+    cached positions and Nq new queries."""
+    name: str
+    dtype: str
+    lengths: List[int]
+    Nq: int
+    H: int
+    Hkv: int
+    d: int
+    page_size: int
+    causal: bool
+    seed: int
+
+    @property
+    def B(self) -> int:
+        return len(self.lengths)
+
+    def flops(self) -> float:
+        return sum(4.0 * self.H * self.Nq * L * self.d for L in self.lengths)
+
+    def bytes(self) -> int:
+        """Bytes a pass must move: every cached K and V row once, Q and O."""
+        kv = sum(self.lengths) * self.Hkv * self.d * 2 * 2
+        return kv + 2 * self.B * self.Nq * self.H * self.d * 2 + 4 * self.B * self.H * self.Nq
+
+
+def paged_decode() -> PagedWorkload:
+    lens = [int(x) for x in uniform_int(1007, 30, 32, 512, 8192)]
+    return PagedWorkload("bf16 paged decode 32 seqs L~U[512,8192] Nq=1 H=32 H_kv=8 d=128 page=64",
+                         "bf16", lens, 1, 32, 8, 128, 64, True, 1007)
+
+
+def make_paged_inputs(w: PagedWorkload) -> dict:
+    """q [B, Nq, H, d]; k_cache, v_cache [pages, page_size, H_kv, d] with the
+    pages of all sequences handed out in a seeded random order (plus two
+    spare pages); block_table int32 [B, max_pages]; seqlens int32 [B]."""
+    conv = to_fp16 if w.dtype == "fp16" else to_bf16
+    P = w.page_size
+    need = [(L + P - 1) // P for L in w.lengths]
+    npages = sum(need) + 2
+    perm = np.argsort(uniform_int(w.seed, 31, npages, 0, 1 << 30), kind="stable")
+    table = np.zeros((w.B, max(need)), dtype=np.int32)
+    used = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[used:used + n]
+        used += n
+    return {"q": conv(normal(w.seed, 0, (w.B, w.Nq, w.H, w.d))),
+            "k_cache": conv(normal(w.seed, 1, (npages, P, w.Hkv, w.d))),
+            "v_cache": conv(normal(w.seed, 2, (npages, P, w.Hkv, w.d))),
+            "block_table": table,
+            "seqlens": np.asarray(w.lengths, dtype=np.int32)}

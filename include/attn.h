@@ -74,6 +74,20 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        attn_dtype_t dtype, void *stream);
 
 /*
+ * Dense attention forward with grouped K/V heads (grouped-query attention;
+ * H_kv = 1 is multi-query attention).  The pages name serving LLMs as the
+ * open target ("optimizing for LLM inference", FlashAttention-3 summary,
+ * arxivlens, Limitations); they do not define the grouping, so this library
+ * takes the usual one: query head h attends with K/V head h / (H / H_kv).
+ *   q, o : [B, N, H, d];  k, v : [B, N, H_kv, d];  lse : [B, H, N] float32
+ *   H_kv : >= 1 and dividing H (else ATTN_ERR_INVALID_ARG).
+ * Everything else as attn_fwd, which is this call with H_kv = H.
+ */
+attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int H_kv, int N, int d, float scale, int causal,
+                           attn_dtype_t dtype, void *stream);
+
+/*
  * Packed variable-length attention forward ("Varlen", named among the
  * features of the HippoAttention case study, streamhpc.com).
  *   cu_seqlens   : DEVICE int32 [nseq + 1]; sequence s occupies tokens
@@ -90,6 +104,15 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
                               const int32_t *cu_seqlens, int nseq, int total_tokens,
                               int max_seqlen, int H, int d, float scale, int causal,
                               attn_dtype_t dtype, void *stream);
+
+/*
+ * attn_fwd_varlen with grouped K/V heads (see attn_fwd_gqa):
+ *   q, o : [T, H, d];  k, v : [T, H_kv, d];  lse : [H, T] float32.
+ */
+attn_status_t attn_fwd_varlen_gqa(const void *q, const void *k, const void *v, void *o,
+                                  float *lse, const int32_t *cu_seqlens, int nseq,
+                                  int total_tokens, int max_seqlen, int H, int H_kv, int d,
+                                  float scale, int causal, attn_dtype_t dtype, void *stream);
 
 /*
  * attn_fwd_varlen without any device allocation.  (The paper has no
@@ -123,6 +146,41 @@ attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, const void *
                                       int total_tokens, int max_seqlen, int H, int d,
                                       float scale, int causal, attn_dtype_t dtype,
                                       int32_t *status, void *stream);
+
+/*
+ * Attention of the newest Nq queries of each sequence against a paged K/V
+ * cache, split over key ranges ("Paged Attention", named among the additions
+ * of the HippoAttention case study, streamhpc.com, "Our approach"; the
+ * FlashAttention-3 summary, arxivlens, Limitations, names LLM inference as
+ * the open target).  Exact attention as in attn_fwd, with grouped K/V heads
+ * (query head h uses K/V head h / (H / H_kv)).
+ *   q            : [B, Nq, H, d];  o : [B, Nq, H, d] (same dtype);
+ *   lse          : [B, H, Nq] float32 (may be NULL).
+ *   k_cache,
+ *   v_cache      : [num_pages, page_size, H_kv, d].  Key position t of
+ *                  sequence b is row t % page_size of page
+ *                  block_table[b * max_pages + t / page_size].
+ *   block_table  : DEVICE int32 [B, max_pages]; entries past a sequence's
+ *                  last page are not read.  Every entry that is read must lie
+ *                  in [0, num_pages): the library does not check the table.
+ *   seqlens_k    : DEVICE int32 [B]; 0 <= seqlens_k[b] <= max_seqlen_k <=
+ *                  max_pages * page_size.
+ *   causal       : the Nq queries are the last Nq positions of the sequence:
+ *                  query i sees keys j <= seqlens_k[b] - Nq + i (a query that
+ *                  sees no key gets O = 0 and lse = -inf).
+ *   num_splits   : key ranges per (sequence, K/V head) computed by separate
+ *                  CTAs and merged (O = sum_s exp(lse_s - lse) O_s); 0 = chosen
+ *                  from the problem size.  The partial results live in a
+ *                  per-device workspace the library allocates on first use
+ *                  and grows when needed.
+ * Limits: d = 64 or 128; (H / H_kv) * Nq <= 16 (ATTN_ERR_UNSUPPORTED
+ * otherwise); any page_size >= 1.
+ */
+attn_status_t attn_fwd_paged(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_table, const int32_t *seqlens_k, void *o,
+                             float *lse, int B, int Nq, int H, int H_kv, int d, int page_size,
+                             int max_pages, int num_pages, int max_seqlen_k, float scale,
+                             int causal, attn_dtype_t dtype, int num_splits, void *stream);
 
 /*
  * 8-bit attention forward (e4m3 operands, block scales).

@@ -92,3 +92,34 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(agb, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         agb.lib()
+
+
+def test_gqa_entry_points_reject_bad_head_counts(L):
+    g = L.attn_fwd_gqa
+    #       q     k     v     o     lse   B  H  Hkv N   d   scale causal dtype stream
+    assert g(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 0, 16, 64, 0.125, 0, 0, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 3, 16, 64, 0.125, 0, 0, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 16, 16, 64, 0.125, 0, 0, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 16, 96, 0.125, 0, 0, None) == 2
+    gv = L.attn_fwd_varlen_gqa
+    assert gv(FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, 10, 8, 8, 3, 64, 0.1, 1, 0, None) == 1
+    assert gv(FAKE, FAKE, FAKE, FAKE, None, None, 2, 10, 8, 8, 2, 64, 0.1, 1, 0, None) == 1
+
+
+def test_paged_entry_point_rejects_bad_arguments(L):
+    p = L.attn_fwd_paged
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=None, B=1, Nq=1, H=8,
+                 Hkv=2, d=128, P=16, maxp=4, npages=8, maxk=64, scale=0.1, causal=1, dtype=0,
+                 splits=0, stream=None)
+        a.update(kw)
+        return p(a["q"], a["k"], a["v"], a["bt"], a["sl"], a["o"], a["lse"], a["B"], a["Nq"],
+                 a["H"], a["Hkv"], a["d"], a["P"], a["maxp"], a["npages"], a["maxk"],
+                 a["scale"], a["causal"], a["dtype"], a["splits"], a["stream"])
+    assert call(bt=None) == 1
+    assert call(Hkv=3) == 1
+    assert call(maxk=65) == 1            # more keys than the table can name
+    assert call(splits=-1) == 1
+    assert call(d=96) == 2
+    assert call(Nq=4, H=8, Hkv=1) == 2   # 32 query rows per K/V head
+    assert call(q=FAKE + 4) == 3

@@ -114,9 +114,10 @@ def test_fp8_attention_rmse_vs_fp64_and_baseline(causal):
 def test_fp8_kernel_arithmetic_on_its_own_inputs():
     """Against the oracle run on the dequantised e4m3 inputs the kernel sees
     (the rotation cancels), the error left is the kernel's own:
-      * P is stored as e4m3(p * w), w = 32 dv_j / dv_max: relative error
-        <= 2^-4 where p*w >= 2^-6 (3 mantissa bits), absolute <= 2^-10 / w
-        below that; the exponential itself is evaluated in fp32;
+      * P is stored as e4m3(p * w), w in [4, 32] the prescale of its key
+        block: relative error <= 2^-4 where p*w >= 2^-6 (3 mantissa bits),
+        absolute <= 2^-10 / w below that; the exponential itself is
+        evaluated in fp32;
       * the row sum l adds the fp32 exponentials in fp32 (eight partial sums
         per row); O is rounded to bf16 (2^-8 relative).
     So |dO| <= 2^-4 A + 2^-8 |O| plus the subnormal term, where A is the
@@ -148,7 +149,9 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     assert np.all(dlse <= lse_tol), float((dlse - lse_tol).max())
     # subnormal P: sum_k 2^-10 / w_min |v_k| / l, with l >= 1 (the largest
     # p of a row is at least 2^0)
-    w_min = 32.0 * (dvn.min(axis=2) / dvn.max(axis=2))             # [B, H]
+    # prescale of every key block: 32 dv_j / dv_max while that stays >= 4,
+    # else the output unit is re-based so that it lies in [4, 32]
+    w_min = np.maximum(4.0, 32.0 * (dvn.min(axis=2) / dvn.max(axis=2)))   # [B, H]
     vsum = np.abs(vd).sum(axis=1)                                   # [B, H, d]
     sub = (2.0 ** -10 / w_min[..., None]) * vsum                    # [B, H, d]
     tol = (2.0 ** -4 + 2.0 ** -8) * a_ref + 2.0 ** -7 * np.abs(o_ref) + sub[:, None] + 1e-5
@@ -175,3 +178,36 @@ def test_fp8_causal_future_keys_are_exactly_masked():
     assert agb.get_status() == 0
     assert torch.equal(o1[:, :r].view(torch.int16), o2[:, :r].view(torch.int16))
     assert torch.equal(l1[:, :, :r].view(torch.int32), l2[:, :, :r].view(torch.int32))
+
+
+def rows_rmse(o, o_ref, rows):
+    return rmse(o[:, rows], o_ref[:, rows])
+
+
+@pytest.mark.parametrize("vmul", [256.0, 16.0])
+def test_fp8_prescale_keeps_range_before_a_large_v_block(vmul):
+    """P is stored as e4m3(p * w) with the V descale of its key block folded
+    into w.  A V block with a much larger scale (a token block whose values
+    are `vmul` times larger) must not cost the other blocks their precision:
+    causal rows before that block never see it, so their error against the
+    fp64 oracle must stay that of the run without the large block (within
+    10%), and below the per-tensor-scale baseline's."""
+    B, N, H, d, blk = 1, 1024, 2, 128, 7
+    q, k, v = outlier_qkv(4500, (B, N, H, d))
+    signs = random_signs(4500, d)
+    vb = v.float()
+    vb[:, blk * 128:(blk + 1) * 128] *= vmul          # a power of two: exact in bf16
+    vb = vb.to(torch.bfloat16)
+    early = slice(0, blk * 128)
+    scale = 1 / math.sqrt(d)
+    o_ref, _ = oracle.attention(q, k, v, scale, True, nthreads=threads())
+    ob_ref, _ = oracle.attention(q, k, vb, scale, True, nthreads=threads())
+    assert np.array_equal(o_ref[:, early], ob_ref[:, early])     # the rows never see it
+    o1, _, _ = fp8_forward(q, k, v, signs, False, causal=True)
+    ob, _, _ = fp8_forward(q, k, vb, signs, False, causal=True)
+    opt, _, _ = fp8_forward(q, k, vb, None, True, causal=True)
+    r1, rb, rpt = (rows_rmse(o, o_ref, early) for o in (o1, ob, opt))
+    print(f"rows before a x{vmul:g} V block: rmse {rb:.3e} (without it {r1:.3e}, "
+          f"per-tensor {rpt:.3e})")
+    assert rb <= 1.1 * r1, (rb, r1)
+    assert rb < rpt, (rb, rpt)
