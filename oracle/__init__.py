@@ -21,6 +21,9 @@ What each function restates:
     through a page table;
   * :func:`merge_partials` -- the combination of softmax results over
     disjoint key sets (split-key decoding), written out from the definition;
+  * :func:`attention_bias` -- the same definition with an additive bias on
+    the scores (the "[+mask]" of the problem statement; "Bias" among the
+    additions of the HippoAttention case study, "Our approach");
   * :func:`rotate`, :func:`hadamard_matrix` -- incoherent processing, same card,
     "8-bit forward pass (FP8, Hopper)": x -> x * diag(signs) * H_d / sqrt(d);
   * :func:`e4m3_encode`, :func:`e4m3_decode`, :func:`block_quant`,
@@ -79,6 +82,10 @@ def _load():
             _dp, _dp, _dp, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_int32, ctypes.c_double, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp,
             _dp, ctypes.c_int32]
+        lib.oracle_attention_rows_bias.argtypes = [
+            _dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _i32p, _i32p,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+            ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp, _dp, ctypes.c_int32]
         lib.oracle_merge_partials.argtypes = [_dp, _dp, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, _dp, _dp]
         lib.oracle_attention_probs.argtypes = [
@@ -208,6 +215,40 @@ def attention_gqa(q, k, v, scale: float, causal: bool, nthreads=None):
     o, lse = attention_varlen_gqa(q.reshape(B * Nq, H, d), k.reshape(B * Nk, Hkv, d),
                                   v.reshape(B * Nk, Hkv, d), cq, ck, scale, causal, nthreads)
     return o.reshape(B, Nq, H, d), lse.reshape(H, B, Nq).transpose(1, 0, 2).copy()
+
+
+def attention_bias(q, k, v, bias, scale: float, causal: bool, nthreads=None):
+    """Dense O [B, N, H, d] and lse [B, H, N] with an additive score bias:
+    s_ij = scale * q_i . k_j + bias[b, h, i, j], bias broadcastable to
+    [B, H, N, N] (numpy broadcasting over the first two axes; a size-1 row
+    axis broadcasts over queries).  -inf removes a key."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    bias = np.asarray(_f64(bias))
+    while bias.ndim < 4:
+        bias = bias[None]
+    sb = 0 if bias.shape[0] == 1 else bias.strides[0] // 8
+    sh = 0 if bias.shape[1] == 1 else bias.strides[1] // 8
+    sr = 0 if bias.shape[2] == 1 else bias.strides[2] // 8
+    if bias.shape[3] != N or bias.strides[3] != 8:
+        raise ValueError("bias keys must be the last, contiguous axis of length N")
+    cu = (np.arange(B + 1) * N).astype(np.int32)
+    tok = np.repeat(np.arange(B * N, dtype=np.int64), H)
+    head = np.tile(np.arange(H, dtype=np.int32), B * N)
+    o = np.empty((tok.shape[0], d), dtype=np.float64)
+    lse = np.empty(tok.shape[0], dtype=np.float64)
+    qq, kk, vv = q.reshape(B * N, H, d), k.reshape(B * N, Hkv, d), v.reshape(B * N, Hkv, d)
+    rc = lib.oracle_attention_rows_bias(_ptr(qq, _dp), _ptr(kk, _dp), _ptr(vv, _dp),
+                                        bias.ctypes.data_as(_dp), sb, sh, sr, _ptr(cu, _i32p),
+                                        _ptr(cu, _i32p), B, H, Hkv, d, float(scale),
+                                        int(bool(causal)), _ptr(tok, _i64p), _ptr(head, _i32p),
+                                        tok.shape[0], _ptr(o, _dp), _ptr(lse, _dp),
+                                        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows_bias failed ({rc})")
+    return o.reshape(B, N, H, d), lse.reshape(B, N, H).transpose(0, 2, 1).copy()
 
 
 def gather_pages(cache, block_table, seqlens):

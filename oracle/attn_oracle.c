@@ -44,6 +44,8 @@
 
 typedef struct {
     const double *q, *k, *v;
+    const double *bias;              /* additive score bias, or NULL */
+    int64_t bias_sb, bias_sh, bias_sr;
     const int32_t *cu, *cuk;
     int32_t nseq, H, Hkv, d, causal;
     double scale;
@@ -106,7 +108,14 @@ static void *rows_worker(void *arg)
             double acc = 0.0;
             for (int32_t c = 0; c < d; ++c) acc += qrow[c] * krow[c];
             sc[j] = jb->scale * acc;
+            if (jb->bias)
+                sc[j] += jb->bias[s * jb->bias_sb + (int64_t)h * jb->bias_sh + i * jb->bias_sr + j];
             if (sc[j] > mx) mx = sc[j];
+        }
+        if (mx == -INFINITY) {       /* every allowed key biased to -inf: no key */
+            for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+            jb->lse[r] = -INFINITY;
+            continue;
         }
         if (nkeys == 0) {            /* no allowed key: O = 0, lse = -inf */
             for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
@@ -140,11 +149,13 @@ static void *rows_worker(void *arg)
  * key gets O = 0, lse = -inf.
  * o: [nrows, d]; lse: [nrows].
  */
-int oracle_attention_rows_gqa(const double *q, const double *k, const double *v,
-                              const int32_t *cu_q, const int32_t *cu_k, int32_t nseq,
-                              int32_t H, int32_t Hkv, int32_t d, double scale, int32_t causal,
-                              const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
-                              double *o, double *lse, int32_t nthreads)
+static int attention_rows_general(const double *q, const double *k, const double *v,
+                                  const double *bias, int64_t bias_sb, int64_t bias_sh,
+                                  int64_t bias_sr, const int32_t *cu_q, const int32_t *cu_k,
+                                  int32_t nseq, int32_t H, int32_t Hkv, int32_t d, double scale,
+                                  int32_t causal, const int64_t *row_tok,
+                                  const int32_t *row_head, int64_t nrows, double *o, double *lse,
+                                  int32_t nthreads)
 {
     if (!q || !k || !v || !cu_q || !cu_k || !row_tok || !row_head || !o || !lse) return -1;
     if (nseq < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1 || nrows < 0) return -1;
@@ -159,6 +170,7 @@ int oracle_attention_rows_gqa(const double *q, const double *k, const double *v,
     for (int32_t w = 0; w < nthreads; ++w) {
         rows_job *jb = &jobs[w];
         jb->q = q; jb->k = k; jb->v = v; jb->cu = cu_q; jb->cuk = cu_k; jb->nseq = nseq;
+        jb->bias = bias; jb->bias_sb = bias_sb; jb->bias_sh = bias_sh; jb->bias_sr = bias_sr;
         jb->H = H; jb->Hkv = Hkv; jb->d = d; jb->causal = causal; jb->scale = scale;
         jb->row_tok = row_tok; jb->row_head = row_head;
         jb->r0 = nrows * w / nthreads; jb->r1 = nrows * (w + 1) / nthreads;
@@ -175,6 +187,36 @@ int oracle_attention_rows_gqa(const double *q, const double *k, const double *v,
         if (jobs[w].status < 0) status = jobs[w].status;
     }
     return status;
+}
+
+int oracle_attention_rows_gqa(const double *q, const double *k, const double *v,
+                              const int32_t *cu_q, const int32_t *cu_k, int32_t nseq,
+                              int32_t H, int32_t Hkv, int32_t d, double scale, int32_t causal,
+                              const int64_t *row_tok, const int32_t *row_head, int64_t nrows,
+                              double *o, double *lse, int32_t nthreads)
+{
+    return attention_rows_general(q, k, v, NULL, 0, 0, 0, cu_q, cu_k, nseq, H, Hkv, d, scale,
+                                  causal, row_tok, row_head, nrows, o, lse, nthreads);
+}
+
+/*
+ * As oracle_attention_rows_gqa with an additive bias on the scores:
+ * s_ij = scale * q_i . k_j + bias[s * sb + h * sh + i * sr + j], s the
+ * sequence, i and j the query and key positions in it (strides in
+ * elements; 0 broadcasts).  A bias of -inf removes a key; a row whose every
+ * allowed key is removed gets O = 0, lse = -inf.
+ */
+int oracle_attention_rows_bias(const double *q, const double *k, const double *v,
+                               const double *bias, int64_t bias_sb, int64_t bias_sh,
+                               int64_t bias_sr, const int32_t *cu_q, const int32_t *cu_k,
+                               int32_t nseq, int32_t H, int32_t Hkv, int32_t d, double scale,
+                               int32_t causal, const int64_t *row_tok, const int32_t *row_head,
+                               int64_t nrows, double *o, double *lse, int32_t nthreads)
+{
+    if (!bias) return -1;
+    return attention_rows_general(q, k, v, bias, bias_sb, bias_sh, bias_sr, cu_q, cu_k, nseq, H,
+                                  Hkv, d, scale, causal, row_tok, row_head, nrows, o, lse,
+                                  nthreads);
 }
 
 /*

@@ -489,3 +489,55 @@ def test_merge_of_key_ranges_equals_unsplit_attention():
     o, lse = oracle.merge_partials(np.stack(parts_o), np.stack(parts_l))
     np.testing.assert_allclose(o, o_full[0].reshape(3 * H, d), rtol=0, atol=1e-13)
     np.testing.assert_allclose(lse, lse_full[0].T.reshape(3 * H), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Additive score bias ("[+mask]" of the problem statement; "Bias" among the
+# additions of the HippoAttention case study, "Our approach")
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bias_matches_torch_sdpa_float64(causal):
+    """A per-(batch, head, query, key) bias against torch's SDPA with the same
+    float mask in float64 (catches a transposed bias or a wrong stride)."""
+    B, N, H, d = 2, 13, 3, 8
+    q, k, v = rnd(60, (B, N, H, d)), rnd(60, (B, N, H, d), 1), rnd(60, (B, N, H, d), 2)
+    bias = 2.0 * rnd(60, (B, H, N, N), 3)
+    o, lse = oracle.attention_bias(q, k, v, bias, 0.35, causal)
+    mask = torch.from_numpy(bias.copy())
+    if causal:
+        mask = mask.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.35)
+    np.testing.assert_allclose(o, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    s = np.einsum("bnhd,bmhd->bhnm", q, k) * 0.35 + mask.numpy()
+    np.testing.assert_allclose(lse, np.logaddexp.reduce(s, axis=3), rtol=0, atol=1e-12)
+
+
+def test_constant_bias_shifts_lse_only():
+    B, N, H, d = 1, 17, 2, 8
+    q, k, v = rnd(61, (B, N, H, d)), rnd(61, (B, N, H, d), 1), rnd(61, (B, N, H, d), 2)
+    o0, l0 = oracle.attention(q, k, v, 0.5, True)
+    o1, l1 = oracle.attention_bias(q, k, v, np.full((1, 1, 1, N), 3.25), 0.5, True)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l1, l0 + 3.25, rtol=0, atol=1e-13)
+
+
+def test_minus_inf_bias_removes_keys():
+    """A key-mask bias (0 or -inf per key, broadcast over heads and queries)
+    equals attention over the kept keys only; a row with every key removed is
+    empty."""
+    B, N, H, d = 2, 20, 2, 8
+    q, k, v = rnd(62, (B, N, H, d)), rnd(62, (B, N, H, d), 1), rnd(62, (B, N, H, d), 2)
+    keep = np.ones((B, N), bool)
+    keep[0, [1, 5, 6, 19]] = False
+    keep[1, 10:] = False
+    bias = np.where(keep, 0.0, -np.inf)[:, None, None, :]
+    o, lse = oracle.attention_bias(q, k, v, bias, 0.4, False)
+    for b in range(B):
+        ob, lb = oracle.attention_gqa(q[b:b + 1], k[b:b + 1, keep[b]], v[b:b + 1, keep[b]], 0.4,
+                                      False)
+        np.testing.assert_allclose(o[b], ob[0], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[b], lb[0], rtol=0, atol=1e-13)
+    o2, l2 = oracle.attention_bias(q, k, v, np.full((1, 1, 1, N), -np.inf), 0.4, False)
+    assert np.all(o2 == 0) and np.all(np.isneginf(l2))
