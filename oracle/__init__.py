@@ -21,6 +21,10 @@ What each function restates:
     through a page table;
   * :func:`merge_partials` -- the combination of softmax results over
     disjoint key sets (split-key decoding), written out from the definition;
+  * :func:`attention_backward` -- the gradients of that definition with
+    respect to Q, K and V, written out from the chain rule (the backward pass
+    the FlashAttention-3 summary's Key Results and the card's "When to use
+    which" refer to);
   * :func:`attention_bias` -- the same definition with an additive bias on
     the scores (the "[+mask]" of the problem statement; "Bias" among the
     additions of the HippoAttention case study, "Our approach");
@@ -86,6 +90,9 @@ def _load():
             _dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _i32p, _i32p,
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
             ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _dp, _dp, ctypes.c_int32]
+        lib.oracle_attention_backward.argtypes = [
+            _dp, _dp, _dp, _dp, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_double, ctypes.c_int32, _dp, _dp, _dp, ctypes.c_int32]
         lib.oracle_merge_partials.argtypes = [_dp, _dp, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, _dp, _dp]
         lib.oracle_attention_probs.argtypes = [
@@ -249,6 +256,26 @@ def attention_bias(q, k, v, bias, scale: float, causal: bool, nthreads=None):
     if rc != 0:
         raise ValueError(f"oracle_attention_rows_bias failed ({rc})")
     return o.reshape(B, N, H, d), lse.reshape(B, N, H).transpose(0, 2, 1).copy()
+
+
+def attention_backward(q, k, v, dout, scale: float, causal: bool, nthreads=None):
+    """Gradients (dq, dk, dv) of the dense forward O = softmax(scale Q K^T) V
+    for an upstream gradient dout: q, dout [B, N, H, d]; k, v [B, N, Hkv, d]."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    cu = (np.arange(B + 1) * N).astype(np.int32)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    rc = lib.oracle_attention_backward(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(do, _dp),
+                                       _ptr(cu, _i32p), B, H, Hkv, d, float(scale),
+                                       int(bool(causal)), _ptr(dq, _dp), _ptr(dk, _dp),
+                                       _ptr(dv, _dp), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_backward failed ({rc})")
+    return dq, dk, dv
 
 
 def gather_pages(cache, block_table, seqlens):

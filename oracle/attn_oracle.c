@@ -236,6 +236,148 @@ int oracle_attention_rows(const double *q, const double *k, const double *v,
                                      causal, row_tok, row_head, nrows, o, lse, nthreads);
 }
 
+/* ------------------------------------------------------------------------ */
+/* Backward pass: gradients of O with respect to Q, K and V.                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * For one sequence and head, with S = scale * Q K^T over the allowed keys and
+ * P = softmax(S) row by row (the forward definition above), O = P V and an
+ * upstream gradient dO:
+ *   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(dO * O)),
+ *   dQ = scale * dS K,   dK = scale * dS^T Q
+ * (rowsum(dO * O) = sum_j P_ij dP_ij, the softmax Jacobian's diagonal term).
+ * Grouped K/V heads: dK and dV of a K/V head sum over its query heads.
+ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    const int32_t *cu;
+    int32_t nseq, H, Hkv, d, causal;
+    double scale;
+    int64_t u0, u1;                 /* (sequence, K/V head) units */
+    double *dq, *dk, *dv;
+    int status;
+} bwd_job;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    const int32_t H = jb->H, Hkv = jb->Hkv, d = jb->d, g = H / Hkv;
+    const int64_t qs = (int64_t)H * d, ks = (int64_t)Hkv * d;
+    int64_t maxlen = 0;
+    for (int32_t s = 0; s < jb->nseq; ++s) {
+        int64_t L = (int64_t)jb->cu[s + 1] - jb->cu[s];
+        if (L > maxlen) maxlen = L;
+    }
+    const size_t LL = (size_t)(maxlen > 0 ? maxlen : 1);
+    double *P = (double *)malloc(sizeof(double) * LL * LL);
+    double *dP = (double *)malloc(sizeof(double) * LL * LL);
+    double *orow = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!P || !dP || !orow) { free(P); free(dP); free(orow); jb->status = -2; return NULL; }
+    for (int64_t u = jb->u0; u < jb->u1; ++u) {
+        const int32_t s = (int32_t)(u / Hkv), hk = (int32_t)(u % Hkv);
+        const int64_t st = jb->cu[s], L = (int64_t)jb->cu[s + 1] - st;
+        for (int32_t gh = 0; gh < g; ++gh) {
+            const int32_t h = hk * g + gh;
+            for (int64_t i = 0; i < L; ++i) {
+                const double *qi = jb->q + (st + i) * qs + (int64_t)h * d;
+                const double *doi = jb->dout + (st + i) * qs + (int64_t)h * d;
+                const int64_t nk = jb->causal ? i + 1 : L;
+                double mx = -INFINITY;
+                for (int64_t j = 0; j < nk; ++j) {
+                    const double *kj = jb->k + (st + j) * ks + (int64_t)hk * d;
+                    double acc = 0.0;
+                    for (int32_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
+                    P[i * L + j] = jb->scale * acc;
+                    if (P[i * L + j] > mx) mx = P[i * L + j];
+                }
+                double z = 0.0;
+                for (int64_t j = 0; j < nk; ++j) { P[i * L + j] = exp(P[i * L + j] - mx); z += P[i * L + j]; }
+                for (int64_t j = 0; j < nk; ++j) P[i * L + j] /= z;
+                for (int64_t j = nk; j < L; ++j) P[i * L + j] = 0.0;
+                /* O_i = sum_j P_ij v_j;  dP_ij = dO_i . v_j;  D_i = dO_i . O_i */
+                for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+                for (int64_t j = 0; j < nk; ++j) {
+                    const double *vj = jb->v + (st + j) * ks + (int64_t)hk * d;
+                    double acc = 0.0;
+                    for (int32_t c = 0; c < d; ++c) { orow[c] += P[i * L + j] * vj[c]; acc += doi[c] * vj[c]; }
+                    dP[i * L + j] = acc;
+                }
+                double Di = 0.0;
+                for (int32_t c = 0; c < d; ++c) Di += doi[c] * orow[c];
+                /* dS_ij = P_ij (dP_ij - D_i), kept in dP */
+                for (int64_t j = 0; j < nk; ++j) dP[i * L + j] = P[i * L + j] * (dP[i * L + j] - Di);
+                for (int64_t j = nk; j < L; ++j) dP[i * L + j] = 0.0;
+                /* dQ_i = scale * sum_j dS_ij k_j */
+                double *dqi = jb->dq + (st + i) * qs + (int64_t)h * d;
+                for (int32_t c = 0; c < d; ++c) dqi[c] = 0.0;
+                for (int64_t j = 0; j < nk; ++j) {
+                    const double *kj = jb->k + (st + j) * ks + (int64_t)hk * d;
+                    for (int32_t c = 0; c < d; ++c) dqi[c] += jb->scale * dP[i * L + j] * kj[c];
+                }
+            }
+            /* dV_j += sum_i P_ij dO_i;  dK_j += scale * sum_i dS_ij q_i */
+            for (int64_t j = 0; j < L; ++j) {
+                double *dvj = jb->dv + (st + j) * ks + (int64_t)hk * d;
+                double *dkj = jb->dk + (st + j) * ks + (int64_t)hk * d;
+                for (int64_t i = 0; i < L; ++i) {
+                    const double pij = P[i * L + j], dsij = dP[i * L + j];
+                    if (pij == 0.0 && dsij == 0.0) continue;
+                    const double *doi = jb->dout + (st + i) * qs + (int64_t)h * d;
+                    const double *qi = jb->q + (st + i) * qs + (int64_t)h * d;
+                    for (int32_t c = 0; c < d; ++c) {
+                        dvj[c] += pij * doi[c];
+                        dkj[c] += jb->scale * dsij * qi[c];
+                    }
+                }
+            }
+        }
+    }
+    free(P); free(dP); free(orow);
+    return NULL;
+}
+
+/*
+ * Gradients for packed sequences: q, dout, dq [T, H, d]; k, v, dk, dv
+ * [T, Hkv, d]; sequence s holds tokens cu_seqlens[s] .. cu_seqlens[s+1]-1.
+ * dk and dv are zeroed here and accumulated over each group's query heads.
+ */
+int oracle_attention_backward(const double *q, const double *k, const double *v,
+                              const double *dout, const int32_t *cu_seqlens, int32_t nseq,
+                              int32_t H, int32_t Hkv, int32_t d, double scale, int32_t causal,
+                              double *dq, double *dk, double *dv, int32_t nthreads)
+{
+    if (!q || !k || !v || !dout || !cu_seqlens || !dq || !dk || !dv) return -1;
+    if (nseq < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1) return -1;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s]) return -1;
+    const int64_t T = cu_seqlens[nseq];
+    memset(dk, 0, sizeof(double) * (size_t)T * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)T * Hkv * d);
+    const int64_t units = (int64_t)nseq * Hkv;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > units) nthreads = (int32_t)units;
+    bwd_job jobs[256];
+    pthread_t th[256];
+    for (int32_t w = 0; w < nthreads; ++w) {
+        bwd_job *jb = &jobs[w];
+        jb->q = q; jb->k = k; jb->v = v; jb->dout = dout; jb->cu = cu_seqlens; jb->nseq = nseq;
+        jb->H = H; jb->Hkv = Hkv; jb->d = d; jb->causal = causal; jb->scale = scale;
+        jb->u0 = units * w / nthreads; jb->u1 = units * (w + 1) / nthreads;
+        jb->dq = dq; jb->dk = dk; jb->dv = dv; jb->status = 0;
+    }
+    for (int32_t w = 1; w < nthreads; ++w)
+        if (pthread_create(&th[w], NULL, bwd_worker, &jobs[w]) != 0) jobs[w].status = -3;
+    bwd_worker(&jobs[0]);
+    int status = jobs[0].status;
+    for (int32_t w = 1; w < nthreads; ++w) {
+        if (jobs[w].status == -3) { jobs[w].status = 0; bwd_worker(&jobs[w]); }
+        else pthread_join(th[w], NULL);
+        if (jobs[w].status < 0) status = jobs[w].status;
+    }
+    return status;
+}
+
 /*
  * Merge of partial results over disjoint key sets of the same query rows
  * (the combine step of attention split over key ranges): with lse_s and

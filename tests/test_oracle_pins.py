@@ -541,3 +541,55 @@ def test_minus_inf_bias_removes_keys():
         np.testing.assert_allclose(lse[b], lb[0], rtol=0, atol=1e-13)
     o2, l2 = oracle.attention_bias(q, k, v, np.full((1, 1, 1, N), -np.inf), 0.4, False)
     assert np.all(o2 == 0) and np.all(np.isneginf(l2))
+
+
+# --------------------------------------------------------------------------
+# Backward pass (FlashAttention-3 summary, Key Results; the card's "When to
+# use which": backward pass needed)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("hkv", [1, 2, 4])
+def test_backward_matches_torch_autograd_float64(hkv, causal):
+    """dQ, dK, dV against torch autograd through float64 SDPA (catches a
+    missing softmax-Jacobian term, a dropped scale, dK/dV not summed over a
+    group's query heads, or gradients leaking through masked keys)."""
+    B, N, H, d = 2, 11, 4, 8
+    q, k, v = rnd(70, (B, N, H, d)), rnd(70, (B, N, hkv, d), 1), rnd(70, (B, N, hkv, d), 2)
+    do = rnd(70, (B, N, H, d), 3)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.3, causal)
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3).requires_grad_() for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.3,
+                                                         enable_gqa=True)
+    o.backward(torch.from_numpy(do).permute(0, 2, 1, 3))
+    for mine, t in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(mine, t.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+
+
+def test_backward_matches_finite_differences_of_the_forward():
+    """Central differences of sum(dO * O) through the oracle's own forward."""
+    B, N, H, d = 1, 6, 1, 4
+    q, k, v, do = (rnd(71, (B, N, H, d), s) for s in range(4))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.7, True)
+    def f(q_, k_, v_):
+        return float((oracle.attention(q_, k_, v_, 0.7, True)[0] * do).sum())
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        for idx in [(0, 0, 0, 0), (0, 3, 0, 2), (0, 5, 0, 3), (0, 2, 0, 1)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            num = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(num - g[idx]) < 1e-7, (idx, num, g[idx])
+
+
+def test_backward_dv_sums_to_do_and_single_key_rows_have_no_dq():
+    """Rows of P sum to 1, so sum_j dV_j = sum_i dO_i; the first causal row
+    has one key, so its softmax is constant and dQ there is 0."""
+    B, N, H, d = 2, 9, 3, 8
+    q, k, v, do = (rnd(72, (B, N, H, d), s) for s in range(4))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.5, True)
+    np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq[:, 0], 0.0, rtol=0, atol=1e-14)
