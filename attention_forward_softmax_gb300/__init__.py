@@ -29,7 +29,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           6: "ATTN_ERR_BAD_SEQLENS", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_TOO_LARGE"}
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_fp8", "qkv_block_quant_hadamard",
            "attn_get_status", "attn_fwd_varlen_noalloc", "attn_fwd_gqa", "attn_fwd_varlen_gqa",
-           "attn_fwd_paged", "attn_status_string", "attn_shutdown", "attn_version")
+           "attn_fwd_paged", "attn_fwd_bias", "attn_bwd", "attn_status_string",
+           "attn_shutdown", "attn_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -72,7 +73,11 @@ def lib() -> ctypes.CDLL:
             L.attn_version.restype = ctypes.c_uint32
             L.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
                                          i, f, i, i, i, vp]
-            for nm in EXPORTS[:9]:
+            ll = ctypes.c_longlong
+            L.attn_fwd_bias.argtypes = [vp, vp, vp, vp, ll, ll, ll, vp, vp, i, i, i, i, i, f, i, i,
+                                        vp]
+            L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+            for nm in EXPORTS[:11]:
                 getattr(L, nm).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -108,10 +113,11 @@ def _need_cuda(*ts):
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-             want_lse: bool = True, stream=None):
+             want_lse: bool = True, stream=None, bias=None):
     """Dense attention, q [B, N, H, d], k/v [B, N, H_kv, d] (H_kv divides H;
     H_kv < H is grouped-query attention), bf16 or fp16
-    -> (o [B,N,H,d], lse [B,H,N] fp32)."""
+    -> (o [B,N,H,d], lse [B,H,N] fp32).  `bias`: optional fp32 tensor
+    broadcastable to [B, H, N, N] added to the scaled scores."""
     _need_cuda(q, k, v)
     B, N, H, d = q.shape
     Hkv = k.shape[2]
@@ -123,7 +129,16 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     _need_cuda(o, lse)
-    if Hkv == H:
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda:
+            raise TypeError("bias must be a float32 CUDA tensor")
+        bv = bias.expand(B, H, N, N)
+        if bv.stride(3) != 1:
+            raise ValueError("bias keys must be contiguous")
+        rc = lib().attn_fwd_bias(_ptr(q), _ptr(k), _ptr(v), bv.data_ptr(), bv.stride(0),
+                                 bv.stride(1), bv.stride(2), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                 scale, int(bool(causal)), _dtype_code(q), _stream(stream))
+    elif Hkv == H:
         rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
                             int(bool(causal)), _dtype_code(q), _stream(stream))
     else:
@@ -208,6 +223,22 @@ def attn_fwd_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen_k: in
                               int(bool(causal)), _dtype_code(q), int(num_splits), _stream(stream))
     _check(rc, "attn_fwd_paged")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             stream=None):
+    """Gradients of the dense forward: q, o, dout [B, N, H, d]; k, v
+    [B, N, H_kv, d]; lse [B, H, N] fp32 from the forward -> (dq, dk, dv)."""
+    _need_cuda(q, k, v, o, lse, dout)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)),
+                        _dtype_code(q), _stream(stream))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool = False,

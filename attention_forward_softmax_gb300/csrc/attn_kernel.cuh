@@ -76,13 +76,18 @@ struct Params {
   int nblk;
   long long wait_budget;
   int *status;
+  const float *bias;        // additive score bias (kBias): bias[b*sb + h*sh + row*sr + key]
+  long long bias_sb, bias_sh, bias_sr;
 };
 
-template <int D_, Elem E_, bool Varlen_>
+template <int D_, Elem E_, bool Varlen_, bool Bias_ = false>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr Elem E = E_;
   static constexpr bool kVarlen = Varlen_;
+  // an fp32 bias added to the scores (16-bit, dense layout)
+  static constexpr bool kBias = Bias_;
+  static_assert(!Bias_ || (E_ != Elem::E4M3 && !Varlen_), "bias: 16-bit dense only");
   static constexpr bool kFp8 = (E_ == Elem::E4M3);
   static constexpr int kElt = kFp8 ? 1 : 2;
   static constexpr int BM = 128;                       // rows per sub-tile
@@ -292,6 +297,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // TMA producer
     // ------------------------------------------------------------------
     if (lane == 0) {
+      // Q is read once per tile; K and V are read again by the CTAs that
+      // work on the other query tiles of the head
+      const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
       int kv_pos = 0, tcount = 0, q_issued = 0;
       bool ok = true;
       TileInfo ti;
@@ -304,9 +312,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int c = 0; c < C::kChunks; ++c) {
             uint8_t *dst = sQ + x * C::kTileBytes + c * C::kChunkBytes;
             if constexpr (C::kVarlen)
-              tma_load_3d(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, ti.start + row);
+              tma_load_3d_hint(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, ti.start + row,
+                               pol_q);
             else
-              tma_load_4d(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, row, ti.b);
+              tma_load_4d_hint(dst, &tmQ, bar_q_full, c * C::kChunkElems, ti.h, row, ti.b, pol_q);
           }
         }
         for (int j = 0; ok && j < ti.nB; ++j) {
@@ -319,11 +328,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int c = 0; c < C::kChunks; ++c) {
               uint8_t *dst = sKV + slot * C::kTileBytes + c * C::kChunkBytes;
               if constexpr (C::kVarlen)
-                tma_load_3d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk,
-                            ti.start + j * 128);
+                tma_load_3d_hint(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk,
+                                 ti.start + j * 128, pol_kv);
               else
-                tma_load_4d(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk, j * 128,
-                            ti.b);
+                tma_load_4d_hint(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk, j * 128,
+                                 ti.b, pol_kv);
             }
           }
         }
@@ -573,8 +582,39 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar_s_free[x]);
         }
-        const float cs = p.scale_log2;   // log2 units per raw score
+        float cs = p.scale_log2;         // log2 units per raw score
         const int kbase = j * 128;
+        if constexpr (C::kBias) {
+          // scores to log2 units with the bias added: s * cs + bias * log2(e);
+          // rows past the end read the last row's bias (their output is not
+          // written), keys past the end are masked below
+          constexpr float kLog2e = 1.4426950408889634f;
+          const float *bp = p.bias + ti.b * p.bias_sb + ti.h * p.bias_sh +
+                            static_cast<long long>(min(row, ti.L - 1)) * p.bias_sr + kbase;
+          if (kbase + 128 <= ti.L) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float4 bv[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) bv[u] = __ldg(reinterpret_cast<const float4 *>(bp + 32 * c) + u);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const float bb[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int i = 32 * c + 4 * u + e;
+                  sv[i] = __float_as_uint(fmaf(__uint_as_float(sv[i]), cs, bb[e] * kLog2e));
+                }
+              }
+            }
+          } else {
+            const int nk = ti.L - kbase;
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (i < nk) sv[i] = __float_as_uint(fmaf(__uint_as_float(sv[i]), cs, __ldg(bp + i) * kLog2e));
+          }
+          cs = 1.f;
+        }
         const bool need_mask = (kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0);
         if (need_mask) {
           const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
@@ -675,7 +715,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            __stcs(dst + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
         }
       }
       if (valid && p.lse != nullptr) {
@@ -875,7 +915,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            __stcs(dst + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
         }
       }
       if (valid && kh == 0 && p.lse != nullptr) {

@@ -63,6 +63,10 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   p.nblk = (a.N + 127) / 128;
   p.wait_budget = a.budget;
   p.status = a.status;
+  p.bias = a.bias;
+  p.bias_sb = a.bias_sb;
+  p.bias_sh = a.bias_sh;
+  p.bias_sr = a.bias_sr;
   const int grid = a.num_tiles < a.num_sms ? a.num_tiles : a.num_sms;
   if (grid <= 0) return ATTN_OK;
   // The shared-memory attribute is set once per device and instantiation;

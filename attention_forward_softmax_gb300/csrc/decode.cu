@@ -16,12 +16,15 @@
 // Design.  Decoding is bound by HBM: each key brings 4 d bytes of K and V
 // and meets only the R = (H / H_kv) * Nq query rows of its K/V head.  So one
 // CTA takes one (sequence, K/V head, key range) and streams that range once:
-//  * 128-key tiles of K and V are gathered row by row through the page table
+//  * 64-key tiles of K and V are gathered row by row through the page table
 //    with 16-byte cp.async copies into XOR-swizzled shared-memory tiles, two
-//    stages deep, so the next tile's rows are in flight while this one is
-//    used;
+//    stages per CTA and three CTAs per SM, so the next tile's rows are in
+//    flight while this one is used (measured: more CTAs per SM beat deeper
+//    stages in fewer CTAs);
+//  * the key range of a sequence is cut into chunks of equal size, one per
+//    CTA, so long and short sequences spread evenly over the SMs;
 //  * the R <= 16 query rows are one 16-row MMA tile; each of the four warps
-//    takes 32 keys of a tile and runs the running-softmax loop on them with
+//    takes 16 keys of a tile and runs the running-softmax loop on them with
 //    warp-level bf16/fp16 MMAs (m16n8k16: S = Q K^T, then O += P V with P
 //    taken from the score registers).  The contractions are tiny -- 16 rows
 //    -- so the tensor pipe is nowhere near the limit; the bytes are;
@@ -40,7 +43,8 @@ namespace attn {
 namespace {
 
 constexpr int kDecThreads = 128;
-constexpr int kTileKeys = 128;     // keys per tile (32 per warp)
+constexpr int kTileKeys = 64;      // keys per tile (16 per warp)
+constexpr int kStages = 2;         // tiles in flight or in use (3 CTAs per SM)
 constexpr int kRows = 16;          // query rows per CTA (one MMA tile)
 
 struct DecodeArgs {
@@ -52,7 +56,9 @@ struct DecodeArgs {
   float *lse;                      // [B, H, Nq] or null
   float *ws_o;                     // [splits, B, H, Nq, d] fp32 partials (splits > 1)
   float *ws_lse;                   // [splits, B, H, Nq]
-  int B, Nq, H, Hkv, page_size, max_pages, num_pages, splits;
+  int B, Nq, H, Hkv, page_size, max_pages, num_pages;
+  int splits;                      // CTAs per (sequence, K/V head): ceil(max_seqlen_k / chunk)
+  int chunk;                       // keys per CTA (a multiple of kTileKeys)
   float scale_log2;
   int causal;
 };
@@ -63,9 +69,9 @@ struct DecSmem {
   static constexpr int kTileBytes = kTileKeys * kRowBytes;     // one K or V tile
   static constexpr int kOffQ = 0;                              // 16 rows
   static constexpr int kOffKV = kRows * kRowBytes;             // [stage][K, V]
-  static constexpr int kBytes = kOffKV + 2 * 2 * kTileBytes;
+  static constexpr int kBytes = kOffKV + kStages * 2 * kTileBytes;
   // after the key loop the K/V area holds the warps' partial results
-  static_assert(4 * kRows * (D + 2) * 4 <= 2 * 2 * kTileBytes, "merge area too small");
+  static_assert(4 * kRows * (D + 2) * 4 <= kStages * 2 * kTileBytes, "merge area too small");
 };
 
 // 16-byte chunk c of row r of a swizzled tile (rows of D 16-bit values):
@@ -131,11 +137,11 @@ __global__ void __launch_bounds__(kDecThreads)
   const int g = a.H / a.Hkv;               // query heads per K/V head
   const int R = g * a.Nq;                  // query rows of this K/V head (<= 16)
   const int Lk = __ldg(a.seqlens_k + b);
-  // key range of this split: whole tiles, the last split takes the rest
-  const int ntiles = (Lk + kTileKeys - 1) / kTileKeys;
-  const int per = (ntiles + a.splits - 1) / a.splits;
-  const int t0 = split * per, t1 = min(ntiles, t0 + per);
-  const int k1 = min(Lk, t1 * kTileKeys);
+  // key range of this CTA: chunk `split` of the sequence (whole tiles)
+  const int k0 = split * a.chunk;
+  if (k0 >= Lk && split > 0) return;       // past the end: the merge does not read it
+  const int k1 = min(Lk, k0 + a.chunk);
+  const int t0 = k0 / kTileKeys, t1 = (k1 + kTileKeys - 1) / kTileKeys;
   const size_t row_stride = static_cast<size_t>(a.Hkv) * D;   // elements between cache rows
   const uint16_t *kc = static_cast<const uint16_t *>(a.k);
   const uint16_t *vc = static_cast<const uint16_t *>(a.v);
@@ -180,14 +186,20 @@ __global__ void __launch_bounds__(kDecThreads)
   const int lim_a = a.causal ? Lk - a.Nq + ra / g : Lk - 1;
   const int lim_b = a.causal ? Lk - a.Nq + rb / g : Lk - 1;
 
-  if (t0 < t1) load_tile(t0, 0);
-  cp_async_commit();
+  // prologue: the first kStages - 1 tiles (one commit group per tile, empty
+  // groups included, so the group count per tile stays fixed)
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (t0 + i < t1) load_tile(t0 + i, i);
+    cp_async_commit();
+  }
   uint32_t qf[D / 16][4];                  // Q fragments, loaded once
   for (int tile = t0; tile < t1; ++tile) {
-    const int stage = (tile - t0) & 1;
-    if (tile + 1 < t1) load_tile(tile + 1, stage ^ 1);
+    const int stage = (tile - t0) % kStages;
+    // refill the stage read one iteration ago (freed by its closing barrier)
+    if (tile + kStages - 1 < t1) load_tile(tile + kStages - 1, (tile - t0 + kStages - 1) % kStages);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<kStages - 1>();
     __syncthreads();
     if (tile == t0) {
 #pragma unroll
@@ -196,26 +208,24 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     const uint32_t kt = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
     const uint32_t vt = kt + L::kTileBytes;
-    const int kw = warp * 32;              // this warp's keys within the tile
-    // S = Q K^T for 32 keys: four 8-key tiles
-    float s[4][4];
+    const int kw = warp * 16;              // this warp's keys within the tile
+    // S = Q K^T for 16 keys: two 8-key tiles (one ldmatrix per k step)
+    float s[2][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {     // two 8-key tiles per ldmatrix
-        uint32_t kb[4];
-        const int key = kw + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        ldsm_x4(kt + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), kb);
-        mma16816<BF16>(s[2 * np], qf[ks], kb[0], kb[1]);
-        mma16816<BF16>(s[2 * np + 1], qf[ks], kb[2], kb[3]);
-      }
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t kb[4];
+      const int key = kw + (lane & 7) + ((lane >> 4) << 3);
+      ldsm_x4(kt + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), kb);
+      mma16816<BF16>(s[0], qf[ks], kb[0], kb[1]);
+      mma16816<BF16>(s[1], qf[ks], kb[2], kb[3]);
+    }
     // mask, then the running softmax in log2 units
     const int kbase = tile * kTileKeys + kw;
     float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = kbase + n * 8 + 2 * tq + e;
@@ -236,9 +246,9 @@ __global__ void __launch_bounds__(kDecThreads)
     m_a = mn_a;
     m_b = mn_b;
     float ps_a = 0.f, ps_b = 0.f;
-    uint32_t pf[2][4];                     // P as A fragments of two 16-key steps
+    uint32_t pf[1][4];                     // P as the A fragment of one 16-key step
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
+    for (int n = 0; n < 2; ++n) {
       const float p0 = ex2(s[n][0] - mu_a), p1 = ex2(s[n][1] - mu_a);
       const float p2 = ex2(s[n][2] - mu_b), p3 = ex2(s[n][3] - mu_b);
       ps_a += p0 + p1;
@@ -257,9 +267,9 @@ __global__ void __launch_bounds__(kDecThreads)
       o[n][2] *= al_b;
       o[n][3] *= al_b;
     }
-    // O += P V: two 16-key steps, d/8 column tiles (two per ldmatrix)
+    // O += P V: one 16-key step, d/8 column tiles (two per ldmatrix)
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks)
+    for (int ks = 0; ks < 1; ++ks)
 #pragma unroll
       for (int np = 0; np < kNT / 2; ++np) {
         uint32_t vb[4];
@@ -354,11 +364,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
   const int rows = a.B * a.H * a.Nq;
   if (row >= rows) return;
   const size_t stride = static_cast<size_t>(rows);
+  // row = (b * H + h) * Nq + qi; sequence b wrote chunks 0 .. ceil(L_b / chunk) - 1
+  const int Lb = __ldg(a.seqlens_k + row / (a.Nq * a.H));
+  const int ns = Lb > 0 ? (Lb + a.chunk - 1) / a.chunk : 1;
   float mx = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) mx = fmaxf(mx, a.ws_lse[s * stride + row]);
+  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, a.ws_lse[s * stride + row]);
   float acc[D / 32] = {}, z = 0.f;
   if (mx != -INFINITY) {
-    for (int s = 0; s < a.splits; ++s) {
+    for (int s = 0; s < ns; ++s) {
       const float w = __expf(a.ws_lse[s * stride + row] - mx);
       z += w;
       const float *po = a.ws_o + (s * stride + row) * D;
@@ -433,19 +446,31 @@ extern "C" attn_status_t attn_fwd_paged(const void *q, const void *k_cache, cons
   DeviceState *ds = nullptr;
   attn_status_t st = device_state(&ds);
   if (st != ATTN_OK) return st;
-  // splits: enough CTAs to cover the SMs twice, at least one 128-key tile each
+  // Chunk of keys per CTA.  Given num_splits, the longest sequence is cut
+  // into that many chunks; otherwise the chunk is sized so that the key rows
+  // of all sequences (at most B * max_seqlen_k) make about 24 CTAs per SM
+  // (eight waves of three), which evens out sequences of different lengths.
   const int tiles = (max_seqlen_k + kTileKeys - 1) / kTileKeys;
-  int splits = num_splits;
-  if (splits == 0) {
-    const long long ctas = static_cast<long long>(B) * H_kv;
-    splits = static_cast<int>((2LL * ds->num_sms + ctas - 1) / ctas);
+  long long chunk_tiles;
+  if (num_splits > 0) {
+    chunk_tiles = (tiles + num_splits - 1) / num_splits;
+  } else {
+    const long long work = static_cast<long long>(B) * H_kv * tiles;
+    chunk_tiles = std::max<long long>(4, (work + 24LL * ds->num_sms - 1) / (24LL * ds->num_sms));
   }
-  splits = std::max(1, std::min(splits, std::min(tiles, 256)));
+  chunk_tiles = std::max<long long>(1, std::min<long long>(chunk_tiles, tiles));
+  int splits = static_cast<int>((tiles + chunk_tiles - 1) / chunk_tiles);
+  if (splits > 1024) {
+    splits = 1024;
+    chunk_tiles = (tiles + splits - 1) / splits;
+    splits = static_cast<int>((tiles + chunk_tiles - 1) / chunk_tiles);
+  }
   DecodeArgs a{};
   a.q = q; a.k = k_cache; a.v = v_cache; a.block_table = block_table; a.seqlens_k = seqlens_k;
   a.o = o; a.lse = lse;
   a.B = B; a.Nq = Nq; a.H = H; a.Hkv = H_kv; a.page_size = page_size; a.max_pages = max_pages;
   a.num_pages = num_pages; a.splits = splits;
+  a.chunk = static_cast<int>(chunk_tiles * kTileKeys);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal ? 1 : 0;
   if (splits > 1) {

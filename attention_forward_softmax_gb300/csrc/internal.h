@@ -25,6 +25,8 @@ struct LaunchArgs {
   const int *num_entries;    // varlen tile-list length (device)
   int num_tiles;             // dense: exact; varlen: upper bound (x H)
   const float *dq, *dk, *dv; // e4m3 descales
+  const float *bias;         // additive score bias (or null)
+  long long bias_sb, bias_sh, bias_sr;
   int *status;
   long long budget;
   int num_sms;
@@ -33,6 +35,7 @@ struct LaunchArgs {
 attn_status_t launch_attn_bf16(const LaunchArgs &a, bool varlen, cudaStream_t s);
 attn_status_t launch_attn_f16(const LaunchArgs &a, bool varlen, cudaStream_t s);
 attn_status_t launch_attn_e4m3(const LaunchArgs &a, cudaStream_t s);
+attn_status_t launch_attn_bias(const LaunchArgs &a, bool bf16, cudaStream_t s);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // dependency on libcuda).  dims/strides/box are innermost-first; strides has
@@ -50,12 +53,15 @@ struct DeviceState {
   size_t tiles_cap = 0;
   float *split_ws = nullptr;    // paged decoding: per-split partial O and lse
   size_t split_ws_bytes = 0;
+  float *bwd_ws = nullptr;      // backward: fp32 dQ accumulator and rowsum(dO * O)
+  size_t bwd_ws_bytes = 0;
   int num_sms = 0;
 };
 attn_status_t device_state(DeviceState **out);
 // Grows the split-key workspace to at least `bytes` (waits for queued work
 // before freeing a smaller one).
 attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes);
+attn_status_t ensure_bwd_workspace(DeviceState *ds, size_t bytes);
 
 // Launches the varlen tile-list builder (one CTA) on `s`.
 cudaError_t launch_varlen_schedule(const int *cu_seqlens, int nseq, int total_tokens,

@@ -68,23 +68,34 @@ attn_status_t ensure_tiles(DeviceState *ds, size_t entries) {
   return ATTN_OK;
 }
 
-attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes) {
+namespace {
+// Grows a cached device buffer to at least `bytes`; the old one may still be
+// used by queued work, so the device is synchronised before it is freed.
+attn_status_t grow_workspace(float **buf, size_t *cap_bytes, size_t bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (ds->split_ws_bytes >= bytes) return ATTN_OK;
-  size_t cap = ds->split_ws_bytes ? ds->split_ws_bytes : (1u << 20);
+  if (*cap_bytes >= bytes) return ATTN_OK;
+  size_t cap = *cap_bytes ? *cap_bytes : (1u << 20);
   while (cap < bytes) cap *= 2;
-  if (ds->split_ws) {
-    // The old workspace may still be used by queued work: wait before freeing.
+  if (*buf) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    cudaFree(ds->split_ws);
-    ds->split_ws = nullptr;
-    ds->split_ws_bytes = 0;
+    cudaFree(*buf);
+    *buf = nullptr;
+    *cap_bytes = 0;
   }
   void *p = nullptr;
   if (cudaMalloc(&p, cap) != cudaSuccess) return ATTN_ERR_CUDA;
-  ds->split_ws = static_cast<float *>(p);
-  ds->split_ws_bytes = cap;
+  *buf = static_cast<float *>(p);
+  *cap_bytes = cap;
   return ATTN_OK;
+}
+}  // namespace
+
+attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes) {
+  return grow_workspace(&ds->split_ws, &ds->split_ws_bytes, bytes);
+}
+
+attn_status_t ensure_bwd_workspace(DeviceState *ds, size_t bytes) {
+  return grow_workspace(&ds->bwd_ws, &ds->bwd_ws_bytes, bytes);
 }
 
 attn_status_t encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr,
@@ -221,6 +232,36 @@ attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o,
   return dtype == ATTN_BF16 ? launch_attn_bf16(a, false, s) : launch_attn_f16(a, false, s);
 }
 
+attn_status_t attn_fwd_bias(const void *q, const void *k, const void *v, const float *bias,
+                            long long bias_stride_b, long long bias_stride_h,
+                            long long bias_stride_row, void *o, float *lse, int B, int H,
+                            int H_kv, int N, int d, float scale, int causal, attn_dtype_t dtype,
+                            void *stream) {
+  attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (!bias || B < 1 || N < 1 || H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (bias_stride_b < 0 || bias_stride_h < 0 || bias_stride_row < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  // every bias row starts on a 16-byte boundary (vector loads)
+  if (!aligned16(bias) || (bias_stride_b & 3) || (bias_stride_h & 3) || (bias_stride_row & 3))
+    return ATTN_ERR_MISALIGNED;
+  const long long tokens = static_cast<long long>(B) * N;
+  const long long tiles = static_cast<long long>(B) * H * ((N + 255) / 256);
+  if (tokens * H * d > (1LL << 40) || tiles > (1LL << 30)) return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  LaunchArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = B; a.H = H; a.Hkv = H_kv; a.N = N; a.d = d;
+  a.T = static_cast<int>(tokens > 0x7fffffff ? 0 : tokens);
+  a.scale = scale; a.causal = causal ? 1 : 0;
+  a.num_tiles = static_cast<int>(tiles);
+  a.bias = bias; a.bias_sb = bias_stride_b; a.bias_sh = bias_stride_h;
+  a.bias_sr = bias_stride_row;
+  a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  return launch_attn_bias(a, dtype == ATTN_BF16, static_cast<cudaStream_t>(stream));
+}
+
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                        int H, int N, int d, float scale, int causal, attn_dtype_t dtype,
                        void *stream) {
@@ -323,11 +364,14 @@ void attn_shutdown(void) {
   cudaGetDevice(&cur);
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState &ds = g_dev[d];
-    if (ds.status == nullptr && ds.tiles == nullptr && ds.split_ws == nullptr) continue;
+    if (ds.status == nullptr && ds.tiles == nullptr && ds.split_ws == nullptr &&
+        ds.bwd_ws == nullptr)
+      continue;
     if (cudaSetDevice(d) != cudaSuccess) continue;
     cudaDeviceSynchronize();
     if (ds.tiles) cudaFree(ds.tiles);
     if (ds.split_ws) cudaFree(ds.split_ws);
+    if (ds.bwd_ws) cudaFree(ds.bwd_ws);
     if (ds.status) cudaFree(ds.status);
     ds = DeviceState{};
   }

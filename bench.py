@@ -59,6 +59,11 @@ def get_workload(name: str):
         return W.varlen_causal()
     if name == "gqa":
         return W.gqa_causal()
+    if name in ("bwd", "bwd_causal"):
+        # the backward pass on the shape of the default workload
+        causal = name == "bwd_causal"
+        return W.Workload(f"bf16 backward {'causal' if causal else 'non-causal'} B=4 H=16 "
+                          f"N=8448 d=128", "bf16", 4, 16, 8448, 128, causal, 1008)
     if name == "paged":
         return W.paged_decode()
     if name.startswith("causal"):
@@ -214,6 +219,18 @@ def build_step(w, dev):
         def step():
             agb.attn_fwd_varlen(q, k, v, cu, max(w.lengths), causal=w.causal, out=o, lse=lse)
         launches = 2   # tile-list builder + attention
+        attn_only, quant_only = step, None
+    elif w.name.startswith("bf16 backward"):
+        # forward once outside the timed region; a step is the backward
+        # (rowsum(dO O) pass, the main kernel, the dQ conversion)
+        o, lse = agb.attn_fwd(q, k, v, causal=w.causal)
+        from datagen import normal, to_bf16
+        do = to_bf16(normal(w.seed, 9, (w.B, w.N, w.H, w.d))).to(dev)
+        flops = 2.5 * w.flops()
+
+        def step():
+            agb.attn_bwd(q, k, v, o, lse, do, causal=w.causal)
+        launches = 3
         attn_only, quant_only = step, None
     else:
         o = torch.empty_like(q)
@@ -403,7 +420,7 @@ def run_gpu(args):
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     exps = flops / (4.0 * w.d)
     mufu_peak = 32.0 * n_sm * sm_mhz * 1e6
-    roof["secondary"] = None if paged else {"bound": "mufu", "achieved": round(exps / (attn_ms / 1e3) / 1e12, 3),
+    roof["secondary"] = None if (paged or w.name.startswith("bf16 backward")) else {"bound": "mufu", "achieved": round(exps / (attn_ms / 1e3) / 1e12, 3),
                          "peak": round(mufu_peak / 1e12, 3), "unit": "Texp/s",
                          "frac": round(exps / (attn_ms / 1e3) / mufu_peak, 4),
                          "peak_source": f"32 exp2 per clock per SM x {n_sm} SMs x "
@@ -456,8 +473,10 @@ def run_gpu(args):
     elif rank == 0:
         value = job_tflops(world, flops, args.steps, t)
         cpu = None if args.no_cpu_baseline else cpu_baseline(w, budget_s=args.cpu_seconds)
+        bwd = w.name.startswith("bf16 backward")
         result = {
-            "metric": "attn fwd TFLOP/s (4*B*H*N^2*d, /2 causal)",
+            "metric": ("attn bwd TFLOP/s (10*B*H*N^2*d, /2 causal)" if bwd else
+                       "attn fwd TFLOP/s (4*B*H*N^2*d, /2 causal)"),
             "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(t / args.steps * 1e3, 4),
@@ -613,7 +632,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="dense",
-                    help="dense | tiny | fp8 | varlen | gqa | paged | causal:N:H:d")
+                    help="dense | tiny | fp8 | varlen | gqa | paged | bwd | bwd_causal | "
+                         "causal:N:H:d")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true",

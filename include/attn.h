@@ -88,6 +88,28 @@ attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o,
                            attn_dtype_t dtype, void *stream);
 
 /*
+ * Dense attention forward with an additive score bias (the "[+mask]" of the
+ * problem; "Bias" among the additions of the HippoAttention case study,
+ * streamhpc.com, "Our approach"):
+ *     S_ij = scale * q_i . k_j + bias[b * sb + h * sh + i * sr + j]
+ * in natural-log units, before the softmax; -inf removes a key (a row with
+ * every allowed key removed gets O = 0, lse = -inf).
+ *   bias : DEVICE float32, keys contiguous; strides sb (batch), sh (head),
+ *          sr (query row) in elements, each >= 0 (0 broadcasts: [1, H, N, N],
+ *          [B, 1, 1, N] key masks, ...).  The bias pointer must be 16-byte
+ *          aligned and every stride a multiple of 4 (ATTN_ERR_MISALIGNED).
+ *   Grouped K/V heads as attn_fwd_gqa (H_kv = H for plain attention).
+ *   Other arguments and layouts as attn_fwd.  The bias is read once per
+ *   (query row, key) pair it applies to, so a full [B, H, N, N] bias makes
+ *   the call bound by its bytes.
+ */
+attn_status_t attn_fwd_bias(const void *q, const void *k, const void *v, const float *bias,
+                            long long bias_stride_b, long long bias_stride_h,
+                            long long bias_stride_row, void *o, float *lse, int B, int H,
+                            int H_kv, int N, int d, float scale, int causal, attn_dtype_t dtype,
+                            void *stream);
+
+/*
  * Packed variable-length attention forward ("Varlen", named among the
  * features of the HippoAttention case study, streamhpc.com).
  *   cu_seqlens   : DEVICE int32 [nseq + 1]; sequence s occupies tokens
@@ -226,6 +248,26 @@ attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void 
                                        float *descale_q, float *descale_k, float *descale_v,
                                        const int8_t *signs, int per_tensor,
                                        int B, int H, int N, int d, void *stream);
+
+/*
+ * Backward pass: gradients of the dense forward (attn_fwd / attn_fwd_gqa)
+ * with respect to Q, K and V, given the upstream gradient dO (the backward
+ * pass of the FlashAttention-3 summary, arxivlens, Key Results; "backward
+ * pass needed" in the "Fused attention kernel" card, "When to use which").
+ * With P the forward's softmax (recomputed from its lse) and
+ * D_i = rowsum(dO_i * O_i):
+ *     dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q
+ * grouped K/V heads sum dK and dV over their query heads.
+ *   q, o, dout, dq : [B, N, H, d];  k, v, dk, dv : [B, N, H_kv, d]
+ *   lse            : [B, H, N] float32, as the forward wrote it.
+ *   d = 128 only (other values: ATTN_ERR_UNSUPPORTED).
+ * The library keeps an fp32 dQ accumulator and the D vector in a per-device
+ * workspace it allocates on first use and grows when needed.
+ */
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                       int H, int H_kv, int N, int d, float scale, int causal,
+                       attn_dtype_t dtype, void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of
