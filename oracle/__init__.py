@@ -24,7 +24,8 @@ What each function restates:
   * :func:`attention_backward` -- the gradients of that definition with
     respect to Q, K and V, written out from the chain rule (the backward pass
     the FlashAttention-3 summary's Key Results and the card's "When to use
-    which" refer to);
+    which" refer to); :func:`attention_backward_rows` gives selected rows of
+    the same gradients for one sequence and K/V head at any length;
   * :func:`attention_bias` -- the same definition with an additive bias on
     the scores (the "[+mask]" of the problem statement; "Bias" among the
     additions of the HippoAttention case study, "Our approach");
@@ -93,6 +94,10 @@ def _load():
         lib.oracle_attention_backward.argtypes = [
             _dp, _dp, _dp, _dp, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_int32, ctypes.c_double, ctypes.c_int32, _dp, _dp, _dp, ctypes.c_int32]
+        lib.oracle_attention_backward_rows.argtypes = [
+            _dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_double, ctypes.c_int32, ctypes.c_int32, _i64p, ctypes.c_int32, _i64p,
+            ctypes.c_int32, _dp, _dp, _dp, ctypes.c_int32]
         lib.oracle_merge_partials.argtypes = [_dp, _dp, ctypes.c_int32, ctypes.c_int64,
                                               ctypes.c_int32, _dp, _dp]
         lib.oracle_attention_probs.argtypes = [
@@ -275,6 +280,30 @@ def attention_backward(q, k, v, dout, scale: float, causal: bool, nthreads=None)
                                        _ptr(dv, _dp), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attention_backward failed ({rc})")
+    return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, dout, scale: float, causal: bool, hk: int, qrows, krows,
+                            nthreads=None):
+    """Selected gradient rows of one sequence at any length: q, dout [L, H, d];
+    k, v [L, Hkv, d].  Returns dq_rows [g, len(qrows), d] for the g query heads
+    of K/V head hk, and dk_rows, dv_rows [len(krows), d] summed over them."""
+    lib = _load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    L, H, d = q.shape
+    Hkv = k.shape[1]
+    g = H // Hkv
+    qr = np.ascontiguousarray(qrows, dtype=np.int64)
+    kr = np.ascontiguousarray(krows, dtype=np.int64)
+    dq = np.empty((g, len(qr), d))
+    dk = np.empty((len(kr), d))
+    dv = np.empty((len(kr), d))
+    rc = lib.oracle_attention_backward_rows(
+        _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(do, _dp), L, H, Hkv, d, float(scale),
+        int(bool(causal)), int(hk), _ptr(qr, _i64p), len(qr), _ptr(kr, _i64p), len(kr),
+        _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_backward_rows failed ({rc})")
     return dq, dk, dv
 
 

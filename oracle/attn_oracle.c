@@ -379,6 +379,152 @@ int oracle_attention_backward(const double *q, const double *k, const double *v,
 }
 
 /*
+ * Selected rows of the same gradients for ONE sequence and ONE K/V head, at
+ * any length: q, dout [L, H, d]; k, v [L, Hkv, d] (one sequence's tokens).
+ * For each query head h of K/V head hk's group (g = H / Hkv heads):
+ *   lse_i and O_i over all queries i (the forward, as above), D_i = dO_i . O_i,
+ *   dQ rows:  dq_rows[h - hk g][r] = scale sum_j P_ij (dO_i . v_j - D_i) k_j,
+ *             i = qrows[r];
+ * and over the group, for j = krows[r]:
+ *   dv_rows[r] = sum_h sum_i P_ij dO_i,
+ *   dk_rows[r] = sum_h sum_i scale P_ij (dO_i . v_j - D_i) q_i.
+ * The first pass (lse, O, D of every query) runs on nthreads threads over
+ * query rows; the selected rows are then summed directly.
+ * dq_rows: [g, nq, d]; dk_rows, dv_rows: [nk, d].
+ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t L, i0, i1;
+    int32_t H, Hkv, d, h, hk, causal;
+    double scale;
+    double *lse, *D;
+} grad_rows_job;
+
+static void *grad_rows_worker(void *arg)
+{
+    grad_rows_job *jb = (grad_rows_job *)arg;
+    const int32_t d = jb->d;
+    const int64_t qs = (int64_t)jb->H * d, ks = (int64_t)jb->Hkv * d;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->L > 0 ? jb->L : 1));
+    double *orow = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!s || !orow) { free(s); free(orow); return (void *)1; }
+    for (int64_t i = jb->i0; i < jb->i1; ++i) {
+        const double *qi = jb->q + i * qs + (int64_t)jb->h * d;
+        const double *doi = jb->dout + i * qs + (int64_t)jb->h * d;
+        const int64_t nk = jb->causal ? i + 1 : jb->L;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < nk; ++j) {
+            const double *kj = jb->k + j * ks + (int64_t)jb->hk * d;
+            double acc = 0.0;
+            for (int32_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
+            s[j] = jb->scale * acc;
+            if (s[j] > mx) mx = s[j];
+        }
+        double z = 0.0;
+        for (int64_t j = 0; j < nk; ++j) { s[j] = exp(s[j] - mx); z += s[j]; }
+        for (int32_t c = 0; c < d; ++c) orow[c] = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+            const double *vj = jb->v + j * ks + (int64_t)jb->hk * d;
+            for (int32_t c = 0; c < d; ++c) orow[c] += (s[j] / z) * vj[c];
+        }
+        double Di = 0.0;
+        for (int32_t c = 0; c < d; ++c) Di += doi[c] * orow[c];
+        jb->lse[i] = mx + log(z);
+        jb->D[i] = Di;
+    }
+    free(s); free(orow);
+    return NULL;
+}
+
+int oracle_attention_backward_rows(const double *q, const double *k, const double *v,
+                                   const double *dout, int64_t L, int32_t H, int32_t Hkv,
+                                   int32_t d, double scale, int32_t causal, int32_t hk,
+                                   const int64_t *qrows, int32_t nq, const int64_t *krows,
+                                   int32_t nk, double *dq_rows, double *dk_rows,
+                                   double *dv_rows, int32_t nthreads)
+{
+    if (!q || !k || !v || !dout || L < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || d < 1) return -1;
+    if (hk < 0 || hk >= Hkv || nq < 0 || nk < 0) return -1;
+    if ((nq > 0 && (!qrows || !dq_rows)) || (nk > 0 && (!krows || !dk_rows || !dv_rows))) return -1;
+    for (int32_t r = 0; r < nq; ++r) if (qrows[r] < 0 || qrows[r] >= L) return -1;
+    for (int32_t r = 0; r < nk; ++r) if (krows[r] < 0 || krows[r] >= L) return -1;
+    const int32_t g = H / Hkv;
+    const int64_t qs = (int64_t)H * d, ks = (int64_t)Hkv * d;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)L);
+    double *D = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!lse || !D) { free(lse); free(D); return -2; }
+    if (nk > 0) {
+        memset(dk_rows, 0, sizeof(double) * (size_t)nk * d);
+        memset(dv_rows, 0, sizeof(double) * (size_t)nk * d);
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > L) nthreads = (int32_t)L;
+    int status = 0;
+    for (int32_t gh = 0; gh < g && status == 0; ++gh) {
+        const int32_t h = hk * g + gh;
+        grad_rows_job jobs[256];
+        pthread_t th[256];
+        int started[256] = {0};
+        for (int32_t w = 0; w < nthreads; ++w) {
+            grad_rows_job *jb = &jobs[w];
+            jb->q = q; jb->k = k; jb->v = v; jb->dout = dout; jb->L = L;
+            jb->i0 = L * w / nthreads; jb->i1 = L * (w + 1) / nthreads;
+            jb->H = H; jb->Hkv = Hkv; jb->d = d; jb->h = h; jb->hk = hk; jb->causal = causal;
+            jb->scale = scale; jb->lse = lse; jb->D = D;
+        }
+        for (int32_t w = 1; w < nthreads; ++w)
+            started[w] = pthread_create(&th[w], NULL, grad_rows_worker, &jobs[w]) == 0;
+        if (grad_rows_worker(&jobs[0]) != NULL) status = -2;
+        for (int32_t w = 1; w < nthreads; ++w) {
+            void *ret = NULL;
+            if (started[w]) pthread_join(th[w], &ret);
+            else ret = grad_rows_worker(&jobs[w]);
+            if (ret != NULL) status = -2;
+        }
+        if (status != 0) break;
+        /* dQ rows of head h */
+        for (int32_t r = 0; r < nq; ++r) {
+            const int64_t i = qrows[r];
+            const double *qi = q + i * qs + (int64_t)h * d;
+            const double *doi = dout + i * qs + (int64_t)h * d;
+            double *out = dq_rows + ((int64_t)gh * nq + r) * d;
+            for (int32_t c = 0; c < d; ++c) out[c] = 0.0;
+            const int64_t nkeys = causal ? i + 1 : L;
+            for (int64_t j = 0; j < nkeys; ++j) {
+                const double *kj = k + j * ks + (int64_t)hk * d;
+                const double *vj = v + j * ks + (int64_t)hk * d;
+                double sij = 0.0, dpij = 0.0;
+                for (int32_t c = 0; c < d; ++c) { sij += qi[c] * kj[c]; dpij += doi[c] * vj[c]; }
+                const double pij = exp(scale * sij - lse[i]);
+                const double dsij = pij * (dpij - D[i]);
+                for (int32_t c = 0; c < d; ++c) out[c] += scale * dsij * kj[c];
+            }
+        }
+        /* dK, dV rows, this head's share */
+        for (int32_t r = 0; r < nk; ++r) {
+            const int64_t j = krows[r];
+            const double *kj = k + j * ks + (int64_t)hk * d;
+            const double *vj = v + j * ks + (int64_t)hk * d;
+            for (int64_t i = causal ? j : 0; i < L; ++i) {
+                const double *qi = q + i * qs + (int64_t)h * d;
+                const double *doi = dout + i * qs + (int64_t)h * d;
+                double sij = 0.0, dpij = 0.0;
+                for (int32_t c = 0; c < d; ++c) { sij += qi[c] * kj[c]; dpij += doi[c] * vj[c]; }
+                const double pij = exp(scale * sij - lse[i]);
+                const double dsij = pij * (dpij - D[i]);
+                for (int32_t c = 0; c < d; ++c) {
+                    dv_rows[(int64_t)r * d + c] += pij * doi[c];
+                    dk_rows[(int64_t)r * d + c] += scale * dsij * qi[c];
+                }
+            }
+        }
+    }
+    free(lse); free(D);
+    return status;
+}
+
+/*
  * Merge of partial results over disjoint key sets of the same query rows
  * (the combine step of attention split over key ranges): with lse_s and
  * O_s the results over part s,

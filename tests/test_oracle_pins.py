@@ -593,3 +593,40 @@ def test_backward_dv_sums_to_do_and_single_key_rows_have_no_dq():
     dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.5, True)
     np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dq[:, 0], 0.0, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_match_torch_autograd_float64(causal):
+    """Selected rows of one sequence's gradients (the form the full-size GPU
+    checks use) against torch autograd through float64 SDPA: every query
+    head of the chosen K/V head's group for dQ, the group sum for dK, dV."""
+    L, H, hkv, d = 37, 6, 2, 8
+    q, do = rnd(73, (1, L, H, d)), rnd(73, (1, L, H, d), 3)
+    k, v = rnd(73, (1, L, hkv, d), 1), rnd(73, (1, L, hkv, d), 2)
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3).requires_grad_() for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.45,
+                                                         enable_gqa=True)
+    o.backward(torch.from_numpy(do).permute(0, 2, 1, 3))
+    gq, gk, gv = (t.grad.permute(0, 2, 1, 3).numpy()[0] for t in (tq, tk, tv))
+    qrows, krows = [0, 1, 17, 36], [0, 5, 35, 36]
+    g = H // hkv
+    for hk in range(hkv):
+        dq, dk, dv = oracle.attention_backward_rows(q[0], k[0], v[0], do[0], 0.45, causal, hk,
+                                                    qrows, krows, nthreads=3)
+        for gh in range(g):
+            np.testing.assert_allclose(dq[gh], gq[qrows, hk * g + gh], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk, gk[krows, hk], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv, gv[krows, hk], rtol=0, atol=1e-12)
+
+
+def test_backward_rows_agree_with_the_full_backward():
+    """The rows entry point and the full backward on the same sequence."""
+    L, H, hkv, d = 50, 4, 1, 16
+    q, k, v, do = (rnd(74, (1, L, h, d), s) for s, h in enumerate((H, hkv, hkv, H)))
+    fq, fk, fv = oracle.attention_backward(q, k, v, do, 0.25, True)
+    rows = list(range(0, L, 7)) + [L - 1]
+    dq, dk, dv = oracle.attention_backward_rows(q[0], k[0], v[0], do[0], 0.25, True, 0, rows,
+                                                rows)
+    np.testing.assert_allclose(dq, fq[0][rows].transpose(1, 0, 2), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, fk[0][rows, 0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, fv[0][rows, 0], rtol=0, atol=1e-13)
