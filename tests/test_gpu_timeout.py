@@ -41,7 +41,22 @@ print("CTX", float(y.sum()))
 """
 
 
-@pytest.mark.parametrize("child", [CHILD, CHILD_FP8], ids=["bf16", "fp8"])
+# the backward kernel: five roles (copies, MMAs, two groups of warps that
+# leave their loops together through named barriers, dQ bulk reduces)
+CHILD_BWD = r"""
+import torch
+import attention_forward_softmax_gb300 as agb
+x = torch.randn(1, 1024, 4, 128, device="cuda").to(torch.bfloat16)
+lse = torch.zeros(1, 4, 1024, device="cuda")
+agb.attn_bwd(x, x, x, x, lse, x, causal=True)
+print("STATUS", agb.get_status())
+print("AGAIN", agb.get_status())
+y = torch.ones(16, device="cuda")
+print("CTX", float(y.sum()))
+"""
+
+
+@pytest.mark.parametrize("child", [CHILD, CHILD_FP8, CHILD_BWD], ids=["bf16", "fp8", "bwd"])
 def test_wait_timeout_is_reported_and_context_survives(child):
     env = dict(os.environ, ATTN_WAIT_BUDGET_CYCLES="1", PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, "-c", child], env=env, capture_output=True, text=True,
