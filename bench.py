@@ -60,10 +60,7 @@ def get_workload(name: str):
     if name == "gqa":
         return W.gqa_causal()
     if name in ("bwd", "bwd_causal"):
-        # the backward pass on the shape of the default workload
-        causal = name == "bwd_causal"
-        return W.Workload(f"bf16 backward {'causal' if causal else 'non-causal'} B=4 H=16 "
-                          f"N=8448 d=128", "bf16", 4, 16, 8448, 128, causal, 1008)
+        return W.backward(name == "bwd_causal")
     if name == "paged":
         return W.paged_decode()
     if name.startswith("causal"):
@@ -224,8 +221,8 @@ def build_step(w, dev):
         # forward once outside the timed region; a step is the backward
         # (rowsum(dO O) pass, the main kernel, the dQ conversion)
         o, lse = agb.attn_fwd(q, k, v, causal=w.causal)
-        from datagen import normal, to_bf16
-        do = to_bf16(normal(w.seed, 9, (w.B, w.N, w.H, w.d))).to(dev)
+        from datagen.workloads import make_dout
+        do = make_dout(w).to(dev)
         flops = 2.5 * w.flops()
 
         def step():

@@ -10,7 +10,9 @@ Recipe (shared by tests, the benchmark and the oracle's timing sample):
     an N(0, 10^2) draw (streams +1000 / +2000 of the same stream), and draws a
     random sign vector of length d for the Hadamard rotation;
   * the varlen workload draws 32 integer lengths uniform on [64, 4096]
-    (stream 10) and packs the sequences back to back.
+    (stream 10) and packs the sequences back to back;
+  * the backward workloads take the dense shape and add the upstream
+    gradient dO, N(0, 1) draws of stream 9 rounded like Q.
 """
 from __future__ import annotations
 
@@ -173,3 +175,15 @@ def make_paged_inputs(w: PagedWorkload) -> dict:
             "v_cache": conv(normal(w.seed, 2, (npages, P, w.Hkv, w.d))),
             "block_table": table,
             "seqlens": np.asarray(w.lengths, dtype=np.int32)}
+
+
+def backward(causal: bool) -> Workload:
+    """The backward pass on the shape of the dense workload."""
+    return Workload(f"bf16 backward {'causal' if causal else 'non-causal'} B=4 H=16 N=8448 d=128",
+                    "bf16", 4, 16, 8448, 128, causal, 1008)
+
+
+def make_dout(w: Workload):
+    """Seeded upstream gradient dO, shaped and rounded like Q."""
+    conv = to_fp16 if w.dtype == "fp16" else to_bf16
+    return conv(normal(w.seed, 9, _shape(w)))
