@@ -18,14 +18,11 @@
 //                 S = Q K^T, P having its own TMEM columns there
 //      warp  9    TMA producer (one thread)
 //      warp 10    d = 64 only: O += P V issuer
-//  * warp roles, e4m3 (608 threads):
-//      warps 0-15 softmax, two threads per row: warp w serves sub-tile
-//                 (w >> 2) & 1 and keys 64 (w >> 3) .. 64 (w >> 3) + 63 of
-//                 each block; warps w and w ^ 8 combine their row maxima
-//                 through shared memory at a pair barrier
-//      warp 16    S = Q K^T issuer + TMEM allocation
-//      warp 17    TMA producer
-//      warp 18    O += P V issuer
+//  * warp roles, e4m3 (352 threads):
+//      warps 0-7  softmax, one thread per row (sub-tile A, then B)
+//      warp  8    S = Q K^T issuer + TMEM allocation
+//      warp  9    TMA producer
+//      warp 10    O += P V issuer
 //  * Q sub-tiles stay in shared memory for the whole tile; K and V tiles of
 //    128 keys stream through a ring of NS slots (K_0, V_0, K_1, V_1, ...);
 //  * TMEM (512 columns): S_A [0,128), S_B [128,256), O_A, O_B after them;
@@ -48,8 +45,7 @@
 //    which rescales O like a grown row max;
 //  * every mbarrier wait is bounded (clock64 budget): on expiry the kernel
 //    records ATTN_ERR_TIMEOUT in the status word, drains its own copies and
-//    MMAs, frees TMEM and returns; the e4m3 pair barriers AND their warps'
-//    wait outcomes, so both warps of a pair leave together.
+//    MMAs, frees TMEM and returns.
 #pragma once
 
 #include "ptx.cuh"
@@ -142,9 +138,8 @@ struct Cfg {
   static constexpr bool kSepP = !kFp8 && D == 64;
   static constexpr uint32_t kColP0 = 256 + 2 * D;        // kSepP: P_X at kColP0 + 64 x
   static constexpr bool kDual = kSmemP || kSepP;         // separate S and O issuers
-  // e4m3: two softmax threads per query row (16 softmax warps)
-  static constexpr bool kSplit = kFp8;
-  static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
+  // softmax warps: one thread per query row of the two sub-tiles
+  static constexpr int kSoftmaxWarps = 8;
   static constexpr int kWarpMMA = kSoftmaxWarps;       // MMA issuer (S = Q K^T) + TMEM allocation
   static constexpr int kWarpTMA = kSoftmaxWarps + 1;   // TMA producer
   static constexpr int kWarpPV = kSoftmaxWarps + 2;    // e4m3: second issuer (O += P V)
@@ -159,11 +154,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
   static constexpr int kNumBars = 2 + 2 * NS + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // e4m3: row maxima [2][2][2][128] and row sums [2][2][128] exchanged by
-  // the two threads of a row
-  static constexpr int kOffRed = (kOffMisc + 64 + 15) / 16 * 16;
-  static constexpr int kRedBytes = kSplit ? (1024 + 512) * 4 : 0;
-  static constexpr int kSmemBytes = kOffRed + kRedBytes + 1024 /* alignment slack */ + 1024 /* guard */;
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeded");
 };
 
@@ -248,7 +239,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *bar_o_free = bar_s_full + 6;           // [2]
   uint64_t *bar_drain = bar_s_full + 8;
   uint64_t *bar_s_free = bar_s_full + 9;           // [2] e4m3: softmax has read S
-  uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3: an O update completed
+  uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3, d = 64: an O update completed
   uint8_t *sP = smem + C::kOffP;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -549,7 +540,187 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_wait_drain(bar_drain, 0);
     }
     __syncwarp();
-  } else if constexpr (!C::kSplit) {
+  } else if constexpr (C::kFp8) {
+    // ------------------------------------------------------------------
+    // e4m3 softmax, one thread per query row: warp w serves sub-tile
+    // x = w >> 2 and TMEM lane quarter w & 3.  The thread reads its whole
+    // 128-key score row, writes its 128-byte row of the P tile (16-byte
+    // chunk c at c ^ (row & 7): the 128-byte swizzle) and owns its row of O.
+    // ------------------------------------------------------------------
+    const int x = warp >> 2;
+    const int wq = warp & 3;
+    const int r_in = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + x * C::kColS;
+    const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
+    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
+    int s_cnt = 0, tcount = 0;
+    unsigned pstore_cnt = 0;
+    bool ok = true;
+    TileInfo ti;
+    for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
+      const int nX = x == 0 ? ti.nA : ti.nB;
+      const int row0 = ti.qt * 256 + x * 128;
+      const int row = row0 + r_in;
+      float m_run = -INFINITY;                          // running max, log2 units
+      float l_run = 0.f;
+      // Per-block descales of this (b, h).  The V descale dv_j of key block
+      // j is folded into P: it is stored as p * w, w = kP8Scale * dv_j / R,
+      // so O accumulates in units of R / kP8Scale.  R starts at the largest
+      // dv of the (b, h); when w would leave [kP8Scale / 8, kP8Scale] (a
+      // block whose scale is far below R, or above it after such a change),
+      // R is re-based to dv_j and O rescaled with it, like the row maximum.
+      const size_t dbase = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
+      const size_t kvbase = (static_cast<size_t>(ti.b) * (p.H / p.grp) + ti.hk) * p.nblk;
+      const float dq_s = __ldg(p.dq + dbase + (row0 >> 7));
+      const float *dk_row = p.dk + kvbase;
+      const float *dv_row = p.dv + kvbase;
+      float dvm = 0.f;
+      for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
+      float r_unit = C::kP8Scale / dvm;                 // kP8Scale / R
+      float dk_next = __ldg(dk_row), dv_next = __ldg(dv_row);
+      for (int j = 0; j < nX; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sv[128];
+        tmem_ld128(tS, sv);
+        // S is in registers: the tensor core may overwrite it
+        tc_fence_before();
+        mbar_arrive(&bar_s_free[x]);
+        const float cs = p.scale_log2 * dq_s * dk_next;   // log2 units per raw score
+        float pw = dv_next * r_unit;
+        float unit_f = 1.f;                                 // O rescale from re-basing R
+        // (the upper test has a little slack so that the block that sets R
+        // does not re-base through rounding; p * w stays below 448 up to
+        // w = 8.3)
+        if (pw < C::kP8Scale * 0.125f || pw > C::kP8Scale * 1.03125f) {   // uniform over (b, h)
+          unit_f = C::kP8Scale / pw;
+          r_unit = C::kP8Scale / dv_next;
+          pw = C::kP8Scale;
+        }
+        if (j + 1 < nX) {
+          dk_next = __ldg(dk_row + j + 1);
+          dv_next = __ldg(dv_row + j + 1);
+        }
+        const int kbase = j * 128;
+        if ((kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0)) {
+          const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
+        }
+        // row maximum: four independent three-input chains
+        float mx4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t *sc = sv + 32 * c;
+          float m = fmaxf(__uint_as_float(sc[0]), __uint_as_float(sc[1]));
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) m = fmax3(m, __uint_as_float(sc[i]), __uint_as_float(sc[i + 1]));
+          mx4[c] = m;
+        }
+        const float m_tile = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool resc = m_new > m_run + C::kRescaleThresh;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m_run - m_new);    // 0 when m_run = -inf
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        // The previous O_X update must be complete before O_X is rescaled
+        // and before its P tile is overwritten.
+        if (pstore_cnt > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc))) {
+          ok = false;
+          break;
+        }
+        ++pstore_cnt;
+        tc_fence_after();
+        // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
+        // into the exponent; row sums of the stored values in packed fp32,
+        // divided by pw once per key block
+        const float lpw = __log2f(fmaxf(pw, 1e-30f));
+        const float mb = m_run - lpw;
+        float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t *sr = sv + 16 * c;
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]), cs, cs, -mb,
+                  -mb);
+            ffma2(x2, x3, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]), cs, cs,
+                  -mb, -mb);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            fadd2(ra[i], rb[i], ra[i], rb[i], p0, p1);
+            fadd2(ra[i], rb[i], ra[i], rb[i], p2, p3);
+            pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          st_shared_v4(p_row + ((c ^ (r_in & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
+                 ex2(-lpw);
+        // Rescale O_X (the previous update has landed, and O_X += P_X(j) V_j
+        // waits for the arrival below).
+        if (j > 0 && (unit_f != 1.f || __any_sync(0xffffffffu, resc))) {
+          const float f = alpha * unit_f;
+#pragma unroll 1
+          for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_p_full[x]);
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O / l, lse ----------------
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_final[x], tcount & 1, wc))) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = row < ti.L;
+      const float inv_l = (l_run > 0.f) ? 1.f / (r_unit * l_run) : 0.f;
+      uint32_t *orow = nullptr;
+      if (valid) {
+        const size_t tok = static_cast<size_t>(ti.start) + row;
+        orow = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(p.o) +
+                                            (tok * p.H + ti.h) * C::D * 2);
+      }
+#pragma unroll 1
+      for (int c = 0; c < C::D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            __stcs(dst + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
+        }
+      }
+      if (valid && p.lse != nullptr) {
+        const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        if constexpr (C::kVarlen)
+          p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
+        else
+          p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.N + row] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_o_free[x]);
+    }
+  } else {
     // ------------------------------------------------------------------
     // 16-bit softmax warpgroups: x = 0 (sub-tile A) or 1 (sub-tile B), one
     // thread per query row
@@ -720,206 +891,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       if (valid && p.lse != nullptr) {
         const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
-        if constexpr (C::kVarlen)
-          p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
-        else
-          p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.N + row] = lse;
-      }
-      tc_fence_before();
-      mbar_arrive(&bar_o_free[x]);
-    }
-  } else {
-    // ------------------------------------------------------------------
-    // e4m3 softmax: two threads per query row.  Warp w serves sub-tile
-    // x = (w >> 2) & 1, key half kh = w >> 3 (keys 64 kh .. 64 kh + 63 of
-    // each block, output columns kh D/2 .. kh D/2 + D/2 - 1) and TMEM lane
-    // quarter wq = w & 3; warps w and w ^ 8 hold the same 32 rows and meet at
-    // pair barrier 1 + 4x + wq once per key block to combine their row
-    // maxima (and at the end of a tile their row sums).  Four softmax warps
-    // share each SM sub-partition.
-    // ------------------------------------------------------------------
-    const int x = (warp >> 2) & 1;
-    const int kh = warp >> 3;
-    const int wq = warp & 3;
-    const int r_in = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + x * C::kColS + kh * 64;
-    const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D + kh * (C::D / 2);
-    const uint32_t pair_bar = 1 + x * 4 + wq;
-    // exchange slots: row maxima [2 slots][x][kh][row], row sums [x][kh][row]
-    float *red_max = reinterpret_cast<float *>(smem + C::kOffRed);
-    float *red_sum = red_max + 2 * 2 * 2 * 128;
-    // this thread's 64 bytes of its row of the P tile: 16-byte chunks
-    // 4 kh .. 4 kh + 3, chunk c of row r stored at c ^ (r & 7) (128-byte swizzle)
-    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
-    int s_cnt = 0, tcount = 0;
-    unsigned pstore_cnt = 0;
-    bool ok = true;
-    TileInfo ti;
-    for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
-      const int nX = x == 0 ? ti.nA : ti.nB;
-      const int row0 = ti.qt * 256 + x * 128;
-      const int row = row0 + r_in;
-      float m_run = -INFINITY;                          // running max, log2 units
-      float l_run = 0.f;                                // this half's running sum
-      // Per-block descales of this (b, h).  The V descale dv_j of key block
-      // j is folded into P: it is stored as p * w, w = kP8Scale * dv_j / R,
-      // so O accumulates in units of R / kP8Scale.  R starts at the largest
-      // dv of the (b, h); when w would leave [kP8Scale / 8, kP8Scale] (a
-      // block whose scale is far below R, or above it after such a change),
-      // R is re-based to dv_j and O rescaled with it, like the row maximum.
-      const size_t dbase = (static_cast<size_t>(ti.b) * p.H + ti.h) * p.nblk;
-      const size_t kvbase = (static_cast<size_t>(ti.b) * (p.H / p.grp) + ti.hk) * p.nblk;
-      const float dq_s = __ldg(p.dq + dbase + (row0 >> 7));
-      const float *dk_row = p.dk + kvbase;
-      const float *dv_row = p.dv + kvbase;
-      float dvm = 0.f;
-      for (int i = lane; i < (ti.L + 127) / 128; i += 32) dvm = fmaxf(dvm, __ldg(dv_row + i));
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
-      float r_unit = C::kP8Scale / dvm;                 // kP8Scale / R
-      float dk_next = __ldg(dk_row), dv_next = __ldg(dv_row);
-      bool good = true;   // every wait of this warp so far succeeded
-      for (int j = 0; j < nX; ++j) {
-        good = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc)) && good;
-        ++s_cnt;
-        tc_fence_after();
-        uint32_t sv[64];
-        tmem_ld64(tS, sv);
-        // S is in registers: the tensor core may overwrite it
-        tc_fence_before();
-        mbar_arrive(&bar_s_free[x]);
-        const float cs = p.scale_log2 * dq_s * dk_next;   // log2 units per raw score
-        float pw = dv_next * r_unit;
-        float unit_f = 1.f;                                 // O rescale from re-basing R
-        // (the upper test has a little slack so that the block that sets R
-        // does not re-base through rounding; p * w stays below 448 up to
-        // w = 8.3)
-        if (pw < C::kP8Scale * 0.125f || pw > C::kP8Scale * 1.03125f) {   // uniform over (b, h)
-          unit_f = C::kP8Scale / pw;
-          r_unit = C::kP8Scale / dv_next;
-          pw = C::kP8Scale;
-        }
-        if (j + 1 < nX) {
-          dk_next = __ldg(dk_row + j + 1);
-          dv_next = __ldg(dv_row + j + 1);
-        }
-        const int kbase = j * 128 + kh * 64;
-        const bool need_mask = (kbase + 64 > ti.L) || (p.causal && kbase + 63 > row0);
-        if (need_mask) {
-          const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
-            if (kbase + 32 + i >= lim) sv[32 + i] = __float_as_uint(-INFINITY);
-          }
-        }
-        float ma = __uint_as_float(sv[0]), mb2 = __uint_as_float(sv[32]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2) {
-          ma = fmax3(ma, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-          mb2 = fmax3(mb2, __uint_as_float(sv[32 + i]), __uint_as_float(sv[33 + i]));
-        }
-        const float pmax = fmax3(ma, __uint_as_float(sv[31]), fmaxf(mb2, __uint_as_float(sv[63])));
-        // combine the two halves' maxima; the barrier also ANDs the wait
-        // outcomes, so both warps of a pair leave together
-        float *slot = red_max + (j & 1) * 512 + x * 256;
-        slot[kh * 128 + r_in] = pmax;
-        if (!named_bar_and(pair_bar, 64, good)) { ok = false; break; }
-        const float mx = fmaxf(pmax, slot[(kh ^ 1) * 128 + r_in]);
-        const float m_tile = mx * cs;
-        const float m_new = fmaxf(m_run, m_tile);
-        const bool resc = m_new > m_run + C::kRescaleThresh;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m_run - m_new);    // 0 when m_run = -inf
-          l_run *= alpha;
-          m_run = m_new;
-        }
-        // The previous O_X update must be complete before O_X is rescaled
-        // and before its P tile is overwritten.
-        if (pstore_cnt > 0)
-          good = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc)) &&
-                 good;
-        ++pstore_cnt;
-        tc_fence_after();
-        // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
-        // into the exponent; row sums of the stored values in packed fp32,
-        // divided by pw once per key block
-        const float lpw = __log2f(fmaxf(pw, 1e-30f));
-        const float mb = m_run - lpw;
-        float ra[4] = {0.f, 0.f, 0.f, 0.f}, rb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t *sr = sv + 32 * half;
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float x0, x1, x2, x3;
-            ffma2(x0, x1, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]), cs, cs, -mb,
-                  -mb);
-            ffma2(x2, x3, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]), cs, cs,
-                  -mb, -mb);
-            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-            fadd2(ra[i & 3], rb[i & 3], ra[i & 3], rb[i & 3], p0, p1);
-            fadd2(ra[(i + 2) & 3], rb[(i + 2) & 3], ra[(i + 2) & 3], rb[(i + 2) & 3], p2, p3);
-            pk[i] = pack_e4m3x4(p0, p1, p2, p3);
-          }
-          const int c0 = 4 * kh + 2 * half;
-          st_shared_v4(p_row + ((c0 ^ (r_in & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-          st_shared_v4(p_row + (((c0 + 1) ^ (r_in & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
-        }
-        fence_proxy_async_smem();
-        l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
-                 ex2(-lpw);
-        // Rescale this half of O_X (the previous update has landed, and
-        // O_X += P_X(j) V_j waits for the arrival below).
-        if (j > 0 && (unit_f != 1.f || __any_sync(0xffffffffu, resc))) {
-          const float f = alpha * unit_f;
-#pragma unroll 1
-          for (int c = 0; c < C::D / 64; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tmem_st32(tO + c * 32, o);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&bar_p_full[x]);
-      }
-      if (!ok) break;
-      // ---------------- epilogue: O / l, lse ----------------
-      good = __all_sync(0xffffffffu, mbar_wait(&bar_o_final[x], tcount & 1, wc)) && good;
-      red_sum[(x * 2 + kh) * 128 + r_in] = l_run;
-      if (!named_bar_and(pair_bar, 64, good)) { ok = false; break; }
-      const float l_row = l_run + red_sum[(x * 2 + (kh ^ 1)) * 128 + r_in];
-      tc_fence_after();
-      const bool valid = row < ti.L;
-      const float inv_l = (l_row > 0.f) ? 1.f / (r_unit * l_row) : 0.f;
-      uint32_t *orow = nullptr;
-      if (valid) {
-        const size_t tok = static_cast<size_t>(ti.start) + row;
-        orow = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(p.o) +
-                                            ((tok * p.H + ti.h) * C::D + kh * (C::D / 2)) * 2);
-      }
-#pragma unroll
-      for (int c = 0; c < C::D / 64; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        if (valid) {
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            __stcs(dst + i, make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]));
-        }
-      }
-      if (valid && kh == 0 && p.lse != nullptr) {
-        const float lse = (m_run + __log2f(l_row)) * 0.69314718055994531f;
         if constexpr (C::kVarlen)
           p.lse[static_cast<size_t>(ti.h) * p.T + ti.start + row] = lse;
         else
