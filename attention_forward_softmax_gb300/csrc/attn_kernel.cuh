@@ -455,24 +455,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           } else {
             for (int j = 0; j < nB; ++j) {
               const unsigned pv = kv_pos + 2 * j + 1;
+              // the V tile and the previous tile's epilogue come first: they
+              // are usually ready long before P, which is then the only
+              // wait between the softmax's arrival and the MMAs
+              if (!wait_kv(pv)) { ok = false; break; }
               if (j < nA) {
+                if (j == 0 && !mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
                 if (!wait_p(0)) { ok = false; break; }
-                if (j == 0) {
-                  if (!mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
-                  tc_fence_after();
-                }
-                if (!wait_kv(pv)) { ok = false; break; }
                 if constexpr (C::kSmemP) issue_pv_smem(0, pv, j > 0);
                 else issue_pv(0, pv, j > 0);
                 mma_commit(&bar_o_done[0]);
                 if (j == nA - 1) mma_commit(&bar_o_final[0]);
               }
+              if (j == 0 && !mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
               if (!wait_p(1)) { ok = false; break; }
-              if (j == 0) {
-                if (!mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
-                tc_fence_after();
-              }
-              if (j >= nA && !wait_kv(pv)) { ok = false; break; }
               if constexpr (C::kSmemP) issue_pv_smem(1, pv, j > 0);
               else issue_pv(1, pv, j > 0);
               mma_commit(&bar_o_done[1]);
