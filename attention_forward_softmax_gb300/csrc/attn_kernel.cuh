@@ -661,8 +661,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           st_shared_v4(p_row + ((c ^ (r_in & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_smem();
-        l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
-                 ex2(-lpw);
         // Rescale O_X (the previous update has landed, and O_X += P_X(j) V_j
         // waits for the arrival below).
         if (j > 0 && (unit_f != 1.f || __any_sync(0xffffffffu, resc))) {
@@ -678,6 +676,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&bar_p_full[x]);
+        // the row sum is not needed by the O update: after the arrival
+        l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
+                 ex2(-lpw);
       }
       if (!ok) break;
       // ---------------- epilogue: O / l, lse ----------------
