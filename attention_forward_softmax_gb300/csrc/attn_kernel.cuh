@@ -74,6 +74,13 @@ struct Params {
   int *status;
   const float *bias;        // additive score bias (kBias): bias[b*sb + h*sh + row*sr + key]
   long long bias_sb, bias_sh, bias_sr;
+  // Dense, non-causal: work items from split_from on (when >= 0) are the
+  // two key halves of the last tiles, so that the final wave of a
+  // persistent grid is not left mostly idle.  Item split_from + u is half
+  // u & 1 of tile split_from + u / 2; it writes O / l (fp32) and its lse to
+  // part u of part_o [parts][256][D] and part_lse [parts][256].
+  int split_from;
+  float *part_o, *part_lse;
 };
 
 template <int D_, Elem E_, bool Varlen_, bool Bias_ = false>
@@ -166,12 +173,20 @@ struct TileInfo {
   int L;          // sequence length
   int start;      // first token of the sequence in the packed / flattened rows
   int nA, nB;     // key tiles processed by sub-tiles A and B
+  int kb0;        // first key tile (a key half of a split tile: nkv / 2)
+  int part;       // split partial written by this item, or -1
 };
 
 template <class C>
 __device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, TileInfo &ti) {
   if (t >= num_tiles) return false;
+  int half = -1;
   if constexpr (!C::kVarlen) {
+    if (p.split_from >= 0 && t >= p.split_from) {   // a key half of a split tile
+      half = (t - p.split_from) & 1;
+      ti.part = t - p.split_from;
+      t = p.split_from + ((t - p.split_from) >> 1);
+    }
     const int nqt = (p.N + 255) / 256;
     const int BH = p.B * p.H;
     int bh;
@@ -207,6 +222,13 @@ __device__ __forceinline__ bool get_tile(const Params &p, int t, int num_tiles, 
     ti.nA = nkv;
     ti.nB = nkv;
   }
+  ti.kb0 = 0;
+  if (half < 0) {
+    ti.part = -1;
+  } else {
+    ti.kb0 = half ? nkv / 2 : 0;
+    ti.nA = ti.nB = half ? nkv - nkv / 2 : nkv / 2;
+  }
   return true;
 }
 
@@ -217,6 +239,31 @@ __device__ __forceinline__ int tile_count(const Params &p) {
   } else {
     return p.num_tiles;
   }
+}
+
+// A key half of a split tile: this thread's row of O / l in fp32 and its lse
+// (natural log, over this half's keys) go to the item's partial.
+template <class C>
+__device__ __forceinline__ void store_partial_row(const Params &p, const TileInfo &ti, int x,
+                                                  int r_in, uint32_t tO, float inv_l,
+                                                  float m_run, float l_run) {
+  const bool valid = ti.qt * 256 + x * 128 + r_in < ti.L;
+  const size_t prow = static_cast<size_t>(ti.part) * 256 + x * 128 + r_in;
+  float *dst = p.part_o + prow * C::D;
+#pragma unroll 1
+  for (int c = 0; c < C::D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + c * 32, o);
+    if (valid) {
+      float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                            __uint_as_float(o[4 * i + 2]) * inv_l,
+                            __uint_as_float(o[4 * i + 3]) * inv_l);
+    }
+  }
+  if (valid) p.part_lse[prow] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
 }
 
 template <class C>
@@ -320,10 +367,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               uint8_t *dst = sKV + slot * C::kTileBytes + c * C::kChunkBytes;
               if constexpr (C::kVarlen)
                 tma_load_3d_hint(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk,
-                                 ti.start + j * 128, pol_kv);
+                                 ti.start + (ti.kb0 + j) * 128, pol_kv);
               else
-                tma_load_4d_hint(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk, j * 128,
-                                 ti.b, pol_kv);
+                tma_load_4d_hint(dst, map, &bar_kv_full[slot], c * C::kChunkElems, ti.hk,
+                                 (ti.kb0 + j) * 128, ti.b, pol_kv);
             }
           }
         }
@@ -576,7 +623,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
       for (int m = 16; m > 0; m >>= 1) dvm = fmaxf(dvm, __shfl_xor_sync(0xffffffffu, dvm, m));
       float r_unit = C::kP8Scale / dvm;                 // kP8Scale / R
-      float dk_next = __ldg(dk_row), dv_next = __ldg(dv_row);
+      float dk_next = __ldg(dk_row + ti.kb0), dv_next = __ldg(dv_row + ti.kb0);
       for (int j = 0; j < nX; ++j) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], s_cnt & 1, wc))) { ok = false; break; }
         ++s_cnt;
@@ -598,10 +645,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           pw = C::kP8Scale;
         }
         if (j + 1 < nX) {
-          dk_next = __ldg(dk_row + j + 1);
-          dv_next = __ldg(dv_row + j + 1);
+          dk_next = __ldg(dk_row + ti.kb0 + j + 1);
+          dv_next = __ldg(dv_row + ti.kb0 + j + 1);
         }
-        const int kbase = j * 128;
+        const int kbase = (ti.kb0 + j) * 128;
         if ((kbase + 128 > ti.L) || (p.causal && kbase + 127 > row0)) {
           const int lim = p.causal ? min(ti.L, row + 1) : ti.L;   // keys < lim allowed
 #pragma unroll
@@ -686,6 +733,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_after();
       const bool valid = row < ti.L;
       const float inv_l = (l_run > 0.f) ? 1.f / (r_unit * l_run) : 0.f;
+      if (ti.part >= 0) {
+        store_partial_row<C>(p, ti, x, r_in, tO, inv_l, m_run, l_run);
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[x]);
+        continue;
+      }
       uint32_t *orow = nullptr;
       if (valid) {
         const size_t tok = static_cast<size_t>(ti.start) + row;
@@ -751,7 +804,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mbar_arrive(&bar_s_free[x]);
         }
         float cs = p.scale_log2;         // log2 units per raw score
-        const int kbase = j * 128;
+        const int kbase = (ti.kb0 + j) * 128;
         if constexpr (C::kBias) {
           // scores to log2 units with the bias added: s * cs + bias * log2(e);
           // rows past the end read the last row's bias (their output is not
@@ -862,6 +915,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_after();
       const bool valid = row < ti.L;
       const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      if (ti.part >= 0) {
+        store_partial_row<C>(p, ti, x, r_in, tO, inv_l, m_run, l_run);
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[x]);
+        continue;
+      }
       uint32_t *orow = nullptr;
       if (valid) {
         const size_t tok = static_cast<size_t>(ti.start) + row;

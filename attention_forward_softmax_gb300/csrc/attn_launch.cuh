@@ -36,6 +36,43 @@ attn_status_t make_qkv_map(CUtensorMap *m, const void *ptr, const LaunchArgs &a,
   }
 }
 
+// Combines the two key halves of each split tile (the running-softmax merge
+// over disjoint key sets): lse = log(e^lse0 + e^lse1), O = e^(lse0 - lse) O0
+// + e^(lse1 - lse) O1, rounded to the output type.  One warp per row.
+template <int D, bool F16Out>
+__global__ void __launch_bounds__(256) split_merge_kernel(const float *part_o, const float *part_lse,
+                                                          void *o, float *lse, int first_tile,
+                                                          int rem, int nqt, int H, int N) {
+  const int w = (blockIdx.x * 256 + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int sidx = w >> 8, r = w & 255;
+  if (sidx >= rem) return;
+  const int t = first_tile + sidx, bh = t / nqt, b = bh / H, h = bh % H;
+  const int row = (t % nqt) * 256 + r;
+  if (row >= N) return;
+  const size_t p0 = (static_cast<size_t>(2 * sidx) * 256 + r), p1 = p0 + 256;
+  const float l0 = part_lse[p0], l1 = part_lse[p1];
+  const float m = fmaxf(l0, l1);
+  const float e0 = expf(l0 - m), e1 = expf(l1 - m);
+  const float inv = 1.f / (e0 + e1);
+  const float w0 = e0 * inv, w1 = e1 * inv;
+  constexpr int kPer = D / 32;                       // 4 (d = 128) or 2 (d = 64)
+  const float *a0 = part_o + p0 * D + lane * kPer, *a1 = part_o + p1 * D + lane * kPer;
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) v[i] = w0 * a0[i] + w1 * a1[i];
+  uint32_t wd[kPer / 2];
+#pragma unroll
+  for (int i = 0; i < kPer / 2; ++i)
+    wd[i] = F16Out ? pack_f16(v[2 * i], v[2 * i + 1]) : pack_bf16(v[2 * i], v[2 * i + 1]);
+  uint16_t *orow = static_cast<uint16_t *>(o) + ((static_cast<size_t>(b) * N + row) * H + h) * D;
+  if constexpr (kPer == 4)
+    *reinterpret_cast<uint2 *>(orow + lane * 4) = make_uint2(wd[0], wd[1]);
+  else
+    *reinterpret_cast<uint32_t *>(orow + lane * 2) = wd[0];
+  if (lane == 0 && lse != nullptr)
+    lse[(static_cast<size_t>(b) * H + h) * N + row] = m + logf(e0 + e1);
+}
+
 template <class C>
 attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
@@ -67,7 +104,13 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   p.bias_sb = a.bias_sb;
   p.bias_sh = a.bias_sh;
   p.bias_sr = a.bias_sr;
-  const int grid = a.num_tiles < a.num_sms ? a.num_tiles : a.num_sms;
+  // dense, non-causal: the last split_rem tiles run as two key halves each
+  const int split_rem = C::kVarlen ? 0 : a.split_rem;
+  p.split_from = split_rem > 0 ? a.num_tiles - split_rem : -1;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  p.num_tiles = a.num_tiles + split_rem;
+  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
   if (grid <= 0) return ATTN_OK;
   // The shared-memory attribute is set once per device and instantiation;
   // concurrent first calls from several host threads are serialised by
@@ -83,7 +126,14 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   });
   if (attr_err[dev] != cudaSuccess) return ATTN_ERR_LAUNCH;
   attn_fwd_kernel<C><<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (split_rem > 0) {
+    const unsigned blocks = static_cast<unsigned>((static_cast<size_t>(split_rem) * 256 * 32 + 255) / 256);
+    split_merge_kernel<C::D, C::E == Elem::F16><<<blocks, 256, 0, s>>>(
+        a.part_o, a.part_lse, a.o, a.lse, p.split_from, split_rem, (a.N + 255) / 256, a.H, a.N);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
 }
 
 }  // namespace attn

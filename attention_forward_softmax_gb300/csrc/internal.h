@@ -30,6 +30,11 @@ struct LaunchArgs {
   int *status;
   long long budget;
   int num_sms;
+  // dense, non-causal: the last split_rem tiles run as two key halves each
+  // (work items num_tiles - split_rem on; num_tiles counts tiles), their
+  // partials in part_o / part_lse; split_rem = 0: no split
+  int split_rem;
+  float *part_o, *part_lse;
 };
 
 attn_status_t launch_attn_bf16(const LaunchArgs &a, bool varlen, cudaStream_t s);
@@ -55,6 +60,8 @@ struct DeviceState {
   size_t split_ws_bytes = 0;
   float *bwd_ws = nullptr;      // backward: fp32 dQ accumulator and rowsum(dO * O)
   size_t bwd_ws_bytes = 0;
+  float *fwd_split_ws = nullptr;  // forward: partials of the split last tiles
+  size_t fwd_split_ws_bytes = 0;
   int num_sms = 0;
 };
 attn_status_t device_state(DeviceState **out);
@@ -62,6 +69,10 @@ attn_status_t device_state(DeviceState **out);
 // before freeing a smaller one).
 attn_status_t ensure_split_workspace(DeviceState *ds, size_t bytes);
 attn_status_t ensure_bwd_workspace(DeviceState *ds, size_t bytes);
+// Dense, non-causal forward: decides whether the last tiles run as key
+// halves (when they would fill at most half of the final wave) and, if so,
+// sets a.split_rem and the partial buffers.
+attn_status_t plan_tail_split(DeviceState *ds, LaunchArgs &a);
 
 // Launches the varlen tile-list builder (one CTA) on `s`.
 cudaError_t launch_varlen_schedule(const int *cu_seqlens, int nseq, int total_tokens,

@@ -98,6 +98,24 @@ attn_status_t ensure_bwd_workspace(DeviceState *ds, size_t bytes) {
   return grow_workspace(&ds->bwd_ws, &ds->bwd_ws_bytes, bytes);
 }
 
+attn_status_t plan_tail_split(DeviceState *ds, LaunchArgs &a) {
+  a.split_rem = 0;
+  if (a.causal || a.num_tiles <= 0 || ds->num_sms <= 0) return ATTN_OK;
+  const int grid = a.num_tiles < ds->num_sms ? a.num_tiles : ds->num_sms;
+  const int rem = a.num_tiles % grid;
+  // worth it only when the last wave is at most half full, and each half
+  // gets at least one key tile
+  if (rem == 0 || 2 * rem > grid || (a.N + 127) / 128 < 2) return ATTN_OK;
+  const size_t rows = static_cast<size_t>(rem) * 2 * 256;
+  attn_status_t st = grow_workspace(&ds->fwd_split_ws, &ds->fwd_split_ws_bytes,
+                                    rows * (a.d + 1) * sizeof(float));
+  if (st != ATTN_OK) return st;
+  a.split_rem = rem;
+  a.part_o = ds->fwd_split_ws;
+  a.part_lse = ds->fwd_split_ws + rows * a.d;
+  return ATTN_OK;
+}
+
 attn_status_t encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr,
                            const cuuint64_t *dims, const cuuint64_t *strides,
                            const cuuint32_t *box, CUtensorMapSwizzle swizzle) {
@@ -228,6 +246,7 @@ attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o,
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.num_tiles = static_cast<int>(tiles);
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  if ((st = plan_tail_split(ds, a)) != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return dtype == ATTN_BF16 ? launch_attn_bf16(a, false, s) : launch_attn_f16(a, false, s);
 }
@@ -259,6 +278,7 @@ attn_status_t attn_fwd_bias(const void *q, const void *k, const void *v, const f
   a.bias = bias; a.bias_sb = bias_stride_b; a.bias_sh = bias_stride_h;
   a.bias_sr = bias_stride_row;
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  if ((st = plan_tail_split(ds, a)) != ATTN_OK) return st;
   return launch_attn_bias(a, dtype == ATTN_BF16, static_cast<cudaStream_t>(stream));
 }
 
@@ -328,6 +348,7 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const
   a.num_tiles = static_cast<int>(tiles);
   a.dq = descale_q; a.dk = descale_k; a.dv = descale_v;
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
+  if ((st = plan_tail_split(ds, a)) != ATTN_OK) return st;
   return launch_attn_e4m3(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -365,13 +386,14 @@ void attn_shutdown(void) {
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState &ds = g_dev[d];
     if (ds.status == nullptr && ds.tiles == nullptr && ds.split_ws == nullptr &&
-        ds.bwd_ws == nullptr)
+        ds.bwd_ws == nullptr && ds.fwd_split_ws == nullptr)
       continue;
     if (cudaSetDevice(d) != cudaSuccess) continue;
     cudaDeviceSynchronize();
     if (ds.tiles) cudaFree(ds.tiles);
     if (ds.split_ws) cudaFree(ds.split_ws);
     if (ds.bwd_ws) cudaFree(ds.bwd_ws);
+    if (ds.fwd_split_ws) cudaFree(ds.fwd_split_ws);
     if (ds.status) cudaFree(ds.status);
     ds = DeviceState{};
   }

@@ -33,10 +33,12 @@
  *    device (a pipeline wait that timed out, malformed cu_seqlens) are
  *    recorded in a device status word read by attn_get_status().
  *  - No call throws, prints, or synchronises (except attn_get_status).
- *  - The library keeps a small per-device workspace (status word, tile list),
- *    allocated on first use and released by attn_shutdown().  Calls that share
- *    a device must be issued from one host thread at a time or be serialised
- *    by the caller.
+ *  - The library keeps a per-device workspace (status word, varlen tile
+ *    list, split partials, backward accumulators), allocated on first use,
+ *    grown when a larger problem needs it and released by attn_shutdown().
+ *    Calls that share a device must be issued from one host thread at a time
+ *    or be serialised by the caller, and calls that use the same workspace
+ *    must not run at the same time on different streams.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -68,6 +70,11 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
  *   scale   : multiplies Q K^T (normally 1/sqrt(d)); must be finite.
  *   causal  : nonzero = query i attends to keys 0..i of its own sequence.
  * The result matches exact attention; S and P stay on chip.
+ * Non-causal shapes whose last wave of 256-row work tiles would fill at most
+ * half of the SMs run those last tiles as two key halves, each writing
+ * O / l and lse in fp32 to the per-device workspace, and a second kernel
+ * merges them (lse = log(e^lse0 + e^lse1), O = sum_i e^(lse_i - lse) O_i).
+ * The same holds for attn_fwd_gqa, attn_fwd_bias and attn_fwd_fp8.
  */
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int H, int N, int d, float scale, int causal,
