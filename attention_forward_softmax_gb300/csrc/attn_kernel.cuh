@@ -70,6 +70,8 @@ struct Params {
   float scale_log2;         // scale * log2(e)
   const float *dq, *dk, *dv;  // e4m3: per-block descales [B,H,nblk] (Q), [B,H_kv,nblk] (K, V)
   int nblk;
+  int d_out;                // head size of the tensors (e4m3: 64 runs the 128-column layout
+                            // with the upper 64 columns of Q, K, V zero-filled by the copies)
   long long wait_budget;
   int *status;
   const float *bias;        // additive score bias (kBias): bias[b*sb + h*sh + row*sr + key]
@@ -743,10 +745,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (valid) {
         const size_t tok = static_cast<size_t>(ti.start) + row;
         orow = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(p.o) +
-                                            (tok * p.H + ti.h) * C::D * 2);
+                                            (tok * p.H + ti.h) * p.d_out * 2);
       }
 #pragma unroll 1
-      for (int c = 0; c < C::D / 32; ++c) {
+      for (int c = 0; c < p.d_out / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         if (valid) {

@@ -22,15 +22,15 @@ template <class C>
 attn_status_t make_qkv_map(CUtensorMap *m, const void *ptr, const LaunchArgs &a, int heads) {
   const cuuint64_t e = C::kElt;
   if constexpr (C::kVarlen) {
-    const cuuint64_t dims[3] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)a.T};
-    const cuuint64_t strides[2] = {C::D * e, (cuuint64_t)heads * C::D * e};
+    const cuuint64_t dims[3] = {(cuuint64_t)a.d, (cuuint64_t)heads, (cuuint64_t)a.T};
+    const cuuint64_t strides[2] = {a.d * e, (cuuint64_t)heads * a.d * e};
     const cuuint32_t box[3] = {(cuuint32_t)C::kChunkElems, 1, 128};
     return encode_tiled(m, tma_dtype<C>(), 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    const cuuint64_t dims[4] = {(cuuint64_t)C::D, (cuuint64_t)heads, (cuuint64_t)a.N,
+    const cuuint64_t dims[4] = {(cuuint64_t)a.d, (cuuint64_t)heads, (cuuint64_t)a.N,
                                 (cuuint64_t)a.B};
-    const cuuint64_t strides[3] = {C::D * e, (cuuint64_t)heads * C::D * e,
-                                   (cuuint64_t)a.N * heads * C::D * e};
+    const cuuint64_t strides[3] = {a.d * e, (cuuint64_t)heads * a.d * e,
+                                   (cuuint64_t)a.N * heads * a.d * e};
     const cuuint32_t box[4] = {(cuuint32_t)C::kChunkElems, 1, 128, 1};
     return encode_tiled(m, tma_dtype<C>(), 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
@@ -98,6 +98,7 @@ attn_status_t launch_cfg(const LaunchArgs &a, cudaStream_t s) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.nblk = (a.N + 127) / 128;
+  p.d_out = a.d;
   p.wait_budget = a.budget;
   p.status = a.status;
   p.bias = a.bias;

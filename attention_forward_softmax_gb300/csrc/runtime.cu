@@ -101,6 +101,7 @@ attn_status_t ensure_bwd_workspace(DeviceState *ds, size_t bytes) {
 attn_status_t plan_tail_split(DeviceState *ds, LaunchArgs &a) {
   a.split_rem = 0;
   if (a.causal || a.num_tiles <= 0 || ds->num_sms <= 0) return ATTN_OK;
+  if (a.dq != nullptr && a.d != 128) return ATTN_OK;   // e4m3 at d = 64: partials are 128 wide
   const int grid = a.num_tiles < ds->num_sms ? a.num_tiles : ds->num_sms;
   const int rem = a.num_tiles % grid;
   // worth it only when the last wave is at most half full, and each half
@@ -334,7 +335,7 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const
   attn_status_t st = check_common(q8, k8, v8, o, lse, H, d, scale);
   if (st != ATTN_OK) return st;
   if (B < 1 || N < 1 || !descale_q || !descale_k || !descale_v) return ATTN_ERR_INVALID_ARG;
-  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return ATTN_ERR_UNSUPPORTED;
   const long long tokens = static_cast<long long>(B) * N;
   const long long tiles = static_cast<long long>(B) * H * ((N + 255) / 256);
   if (tokens * H * d > (1LL << 40) || tiles > (1LL << 30)) return ATTN_ERR_TOO_LARGE;

@@ -55,6 +55,9 @@ def get_workload(name: str):
         return W.TINY
     if name == "fp8":
         return W.FP8
+    if name == "fp8_d64":
+        return W.Workload("fp8 e4m3 non-causal B=4 H=16 N=8192 d=64, 0.1% outliers", "fp8",
+                          4, 16, 8192, 64, False, 1003, outliers=True)
     if name == "varlen":
         return W.varlen_causal()
     if name == "gqa":
@@ -629,7 +632,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="dense",
-                    help="dense | tiny | fp8 | varlen | gqa | paged | bwd | bwd_causal | "
+                    help="dense | tiny | fp8 | fp8_d64 | varlen | gqa | paged | bwd | bwd_causal | "
                          "causal:N:H:d")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -25,8 +25,8 @@
  *        dense  lse        : [B, H, N] float32
  *        varlen Q, K, V, O : [T, H, d]     (sequences packed back to back)
  *        varlen lse        : [H, T] float32
- *  - Supported head dimensions: d = 64 and d = 128 (attn_fwd_fp8: d = 128
- *    only; other values return ATTN_ERR_UNSUPPORTED).
+ *  - Supported head dimensions: d = 64 and d = 128 (attn_bwd: d = 128 only;
+ *    other values return ATTN_ERR_UNSUPPORTED).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call is asynchronous on that stream; the return value reports
  *    argument validation and launch errors only.  Errors detected on the
@@ -222,8 +222,9 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_cache, const void *v_c
  *                below writes 1 for an all-zero block); other values give
  *                undefined output.
  *   o   : [B, N, H, d] bf16;  lse : [B, H, N] float32 (may be NULL).
- *   d   : 128 (an e4m3 row is then one 128-byte swizzle row); d = 64 returns
- *         ATTN_ERR_UNSUPPORTED.
+ *   d   : 128, or 64: a 64-byte row is copied into a 128-byte swizzle row
+ *         whose upper half the copy fills with zeros, so d = 64 runs the
+ *         d = 128 kernel (twice the tensor work per useful flop).
  * V is consumed in its stored [token, d] layout (no transpose in memory).
  */
 attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8,

@@ -78,7 +78,7 @@ def test_varlen_fp8_quant_reject_bad_arguments(L):
     assert v(FAKE, FAKE, FAKE, FAKE, None, FAKE + 2, 2, 10, 8, 1, 64, 0.1, 1, 0, None) == 3
     f = L.attn_fwd_fp8
     assert f(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 1, 1, 16, 128, 0.1, 0, None) == 1
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 16, 64, 0.1, 0, None) == 2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 16, 96, 0.1, 0, None) == 2
     qz = L.qkv_block_quant_hadamard
     assert qz(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0, 1, 1, 16, 64, None) == 1
     assert qz(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, 1, 16, 48, None) == 2

@@ -95,23 +95,45 @@ def rmse(a, b):
     return float(np.sqrt(np.mean((np.asarray(a, np.float64) - b) ** 2)))
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_attention_rmse_vs_fp64_and_baseline(causal):
+def test_fp8_attention_rmse_vs_fp64_and_baseline(causal, d):
     """Block scales + incoherent processing vs the per-tensor baseline, both
-    measured against the fp64 oracle on the unrotated bf16 inputs."""
-    B, N, H, d = 2, 1000, 4, 128
+    measured against the fp64 oracle on the unrotated bf16 inputs.  The
+    absolute bar (1.2e-2) is held at d = 128.  At d = 64 the method's input
+    quantisation alone -- the oracle's own block quantisation and rotation,
+    then exact fp64 attention on the dequantised inputs -- is already above
+    it on this distribution (half the values per 128-token block, an outlier
+    spread over 64 rotated channels instead of 128: 1.29e-2 against 8.1e-3
+    at d = 128), so there the kernel is held to 1.2 x that floor and to the
+    per-tensor baseline.  The kernel's own error on its dequantised inputs
+    (RMSE about 4e-3, element-wise within the e4m3 bound of the arithmetic
+    test below) is independent of the input quantisation and adds in
+    quadrature: sqrt(1.29e-2^2 + 4e-3^2) = 1.35e-2 < 1.2 x 1.29e-2."""
+    B, N, H = 2, 1000, 4
     q, k, v = outlier_qkv(4200, (B, N, H, d))
     signs = random_signs(4200, d)
-    o_ref, lse_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), causal, nthreads=threads())
+    scale = 1 / math.sqrt(d)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal, nthreads=threads())
     o_blk, lse_blk, _ = fp8_forward(q, k, v, signs, False, causal)
     o_pt, _, _ = fp8_forward(q, k, v, None, True, causal)
     r_blk, r_pt = rmse(o_blk, o_ref), rmse(o_pt, o_ref)
-    assert r_blk <= 1.2e-2, r_blk
+    qz = oracle.quantize_qkv(q, k, v, signs)
+    deq = [oracle.dequantize(qz[n + "8"], qz["d" + n]) for n in "qkv"]
+    o_floor, _ = oracle.attention(*deq, scale, causal, nthreads=threads())
+    r_floor = rmse(o_floor, o_ref)
+    print(f"fp8 d={d} causal={causal}: rmse {r_blk:.3e}, quantisation floor {r_floor:.3e}, "
+          f"per-tensor {r_pt:.3e}")
+    if d == 128:
+        assert r_blk <= 1.2e-2, r_blk
+    else:
+        assert r_blk <= 1.2 * r_floor, (r_blk, r_floor)
     assert r_blk < r_pt, (r_blk, r_pt)
     assert np.isfinite(lse_blk).all()
 
 
-def test_fp8_kernel_arithmetic_on_its_own_inputs():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_kernel_arithmetic_on_its_own_inputs(d):
     """Against the oracle run on the dequantised e4m3 inputs the kernel sees
     (the rotation cancels), the error left is the kernel's own:
       * P is stored as e4m3(p * w), w in [1, 8] the prescale of its key
@@ -127,7 +149,7 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     relative error below 2^-21, and l collects at most N/16 + 8 roundings of
     2^-24 relative; |dlse| is bounded by the largest score error plus the
     relative error of l."""
-    B, N, H, d = 1, 700, 2, 128
+    B, N, H = 1, 700, 2
     q, k, v = outlier_qkv(4300, (B, N, H, d))
     signs = random_signs(4300, d)
     o, lse, (q8, k8, v8, dq, dk, dv) = fp8_forward(q, k, v, signs, False)
@@ -160,12 +182,13 @@ def test_fp8_kernel_arithmetic_on_its_own_inputs():
     print(f"fp8 kernel vs oracle on its own inputs: rmse {rmse(o, o_ref):.3e}")
 
 
-def test_fp8_causal_future_keys_are_exactly_masked():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_causal_future_keys_are_exactly_masked(d):
     """Poison the e4m3 codes of every key at or beyond row r (K = NaN code
     0x7f, V = +-448 codes 0x7e / 0xfe; the descales are unchanged): outputs of
     rows < r are bitwise identical to the clean run, so masking is by select
-    in both halves of the two-threads-per-row softmax."""
-    B, N, H, d, r = 2, 400, 2, 128, 190
+    before the exponential."""
+    B, N, H, r = 2, 400, 2, 190
     q, k, v = outlier_qkv(4400, (B, N, H, d))
     q8, k8, v8, dq, dk, dv = agb.qkv_block_quant_hadamard(q.cuda(), k.cuda(), v.cuda(), None)
     o1, l1 = agb.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=True)
