@@ -62,6 +62,12 @@ struct DeviceState {
   size_t bwd_ws_bytes = 0;
   float *fwd_split_ws = nullptr;  // forward: partials of the split last tiles
   size_t fwd_split_ws_bytes = 0;
+  // host-buffer forward (attn_fwd_host): two device staging sets, the copy
+  // streams and the events that order copies and compute
+  float *host_ws = nullptr;
+  size_t host_ws_bytes = 0;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
   int num_sms = 0;
 };
 attn_status_t device_state(DeviceState **out);

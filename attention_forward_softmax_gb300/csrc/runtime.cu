@@ -289,6 +289,80 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
   return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, dtype, stream);
 }
 
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            attn_dtype_t dtype, void *stream) {
+  attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  const size_t per_b = static_cast<size_t>(N) * H * d * 2;        // q, k, v or o of one entry
+  const size_t lse_b = static_cast<size_t>(H) * N * sizeof(float);
+  if (static_cast<long long>(N) * H * d > (1LL << 40) / B) return ATTN_ERR_TOO_LARGE;
+  // one staging set: q, k, v, o and lse of one batch entry, 256-byte aligned parts
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t set_bytes = 4 * up(per_b) + up(lse_b);
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  if ((st = grow_workspace(&ds->host_ws, &ds->host_ws_bytes, 2 * set_bytes)) != ATTN_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (ds->h2d == nullptr) {
+      if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ds->ev_start, cudaEventDisableTiming) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      for (int i = 0; i < 2; ++i)
+        if (cudaEventCreateWithFlags(&ds->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ds->ev_comp[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ds->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+          return ATTN_ERR_CUDA;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char *qh = static_cast<const char *>(q), *kh = static_cast<const char *>(k);
+  const char *vh = static_cast<const char *>(v);
+  char *oh = static_cast<char *>(o);
+  char *ws = reinterpret_cast<char *>(ds->host_ws);
+  bool ok = true;
+  auto chk = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // everything queued on the caller's stream before this call comes first
+  chk(cudaEventRecord(ds->ev_start, s));
+  chk(cudaStreamWaitEvent(ds->h2d, ds->ev_start, 0));
+  for (int c = 0; ok && c < B; ++c) {
+    const int set = c & 1;
+    char *dq = ws + set * set_bytes, *dk = dq + up(per_b), *dv = dk + up(per_b);
+    char *dout = dv + up(per_b);
+    float *dlse = reinterpret_cast<float *>(dout + up(per_b));
+    // inputs of entry c, once entry c - 2 (same set) has been computed (one
+    // copy stream: a second one measured slower, the two share the host link)
+    if (c >= 2) chk(cudaStreamWaitEvent(ds->h2d, ds->ev_comp[set], 0));
+    chk(cudaMemcpyAsync(dq, qh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpyAsync(dk, kh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpyAsync(dv, vh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaEventRecord(ds->ev_in[set], ds->h2d));
+    // compute on the caller's stream, once the inputs are in and entry c - 2's
+    // outputs have left the set
+    chk(cudaStreamWaitEvent(s, ds->ev_in[set], 0));
+    if (c >= 2) chk(cudaStreamWaitEvent(s, ds->ev_out[set], 0));
+    if (!ok) break;
+    if ((st = attn_fwd_gqa(dq, dk, dv, dout, lse ? dlse : nullptr, 1, H, H, N, d, scale, causal,
+                           dtype, stream)) != ATTN_OK)
+      return st;
+    chk(cudaEventRecord(ds->ev_comp[set], s));
+    // outputs of entry c
+    chk(cudaStreamWaitEvent(ds->d2h, ds->ev_comp[set], 0));
+    chk(cudaMemcpyAsync(oh + c * per_b, dout, per_b, cudaMemcpyDeviceToHost, ds->d2h));
+    if (lse) chk(cudaMemcpyAsync(lse + static_cast<size_t>(c) * H * N, dlse, lse_b,
+                                 cudaMemcpyDeviceToHost, ds->d2h));
+    chk(cudaEventRecord(ds->ev_out[set], ds->d2h));
+  }
+  // later work on the caller's stream sees the outputs (the copy-out stream
+  // runs in order, so its last event covers every entry)
+  if (ok) chk(cudaStreamWaitEvent(s, ds->ev_out[(B - 1) & 1], 0));
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t attn_fwd_varlen_gqa(const void *q, const void *k, const void *v, void *o,
                                   float *lse, const int32_t *cu_seqlens, int nseq,
                                   int total_tokens, int max_seqlen, int H, int H_kv, int d,
@@ -387,7 +461,7 @@ void attn_shutdown(void) {
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState &ds = g_dev[d];
     if (ds.status == nullptr && ds.tiles == nullptr && ds.split_ws == nullptr &&
-        ds.bwd_ws == nullptr && ds.fwd_split_ws == nullptr)
+        ds.bwd_ws == nullptr && ds.fwd_split_ws == nullptr && ds.host_ws == nullptr)
       continue;
     if (cudaSetDevice(d) != cudaSuccess) continue;
     cudaDeviceSynchronize();
@@ -395,6 +469,15 @@ void attn_shutdown(void) {
     if (ds.split_ws) cudaFree(ds.split_ws);
     if (ds.bwd_ws) cudaFree(ds.bwd_ws);
     if (ds.fwd_split_ws) cudaFree(ds.fwd_split_ws);
+    if (ds.host_ws) cudaFree(ds.host_ws);
+    for (int i = 0; i < 2; ++i) {
+      if (ds.ev_in[i]) cudaEventDestroy(ds.ev_in[i]);
+      if (ds.ev_comp[i]) cudaEventDestroy(ds.ev_comp[i]);
+      if (ds.ev_out[i]) cudaEventDestroy(ds.ev_out[i]);
+    }
+    if (ds.ev_start) cudaEventDestroy(ds.ev_start);
+    if (ds.h2d) cudaStreamDestroy(ds.h2d);
+    if (ds.d2h) cudaStreamDestroy(ds.d2h);
     if (ds.status) cudaFree(ds.status);
     ds = DeviceState{};
   }

@@ -76,6 +76,11 @@ def test_varlen_fp8_quant_reject_bad_arguments(L):
     assert v(FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, 10, 8, 1, 64, 0.1, 1, 0, None) == 1
     assert v(FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, 10, 8, 1, 80, 0.1, 1, 0, None) == 2
     assert v(FAKE, FAKE, FAKE, FAKE, None, FAKE + 2, 2, 10, 8, 1, 64, 0.1, 1, 0, None) == 3
+    hst = L.attn_fwd_host
+    assert hst(None, FAKE, FAKE, FAKE, None, 2, 4, 16, 64, 0.1, 0, 0, None) == 1
+    assert hst(FAKE, FAKE, FAKE, FAKE, None, 0, 4, 16, 64, 0.1, 0, 0, None) == 1
+    assert hst(FAKE, FAKE, FAKE, FAKE, None, 2, 4, 16, 96, 0.1, 0, 0, None) == 2
+    assert hst(FAKE, FAKE, FAKE + 4, FAKE, None, 2, 4, 16, 64, 0.1, 0, 0, None) == 3
     f = L.attn_fwd_fp8
     assert f(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 1, 1, 16, 128, 0.1, 0, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 16, 96, 0.1, 0, None) == 2

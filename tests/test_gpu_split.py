@@ -57,12 +57,13 @@ def sample(N, H, first_split, seed):
     return np.array(toks, np.int64), np.array(heads, np.int32)
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float16, 128),
-                                     (torch.bfloat16, 64)])
-def test_split_tail_16bit(dtype, d):
+@pytest.mark.parametrize("dtype,d,grp", [(torch.bfloat16, 128, 1), (torch.float16, 128, 1),
+                                         (torch.bfloat16, 64, 1), (torch.bfloat16, 128, 2)])
+def test_split_tail_16bit(dtype, d, grp):
     N = 4096
     H, first_split, T = split_shape(N)
-    q, k, v = qkv(9100 + d, (1, N, H, d), dtype)
+    q, _, _ = qkv(9100 + d, (1, N, H, d), dtype)
+    _, k, v = qkv(9150 + d + grp, (1, N, H // grp, d), dtype)
     o, lse = agb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
     torch.cuda.synchronize()
     assert agb.get_status() == 0
@@ -70,14 +71,16 @@ def test_split_tail_16bit(dtype, d):
     cu = np.array([0, N], np.int32)
     q2, k2, v2 = (x[0].to(torch.float64).numpy() for x in (q, k, v))
     scale = 1 / math.sqrt(d)
-    o_ref, lse_ref = oracle.attention_rows(q2, k2, v2, cu, scale, False, toks, heads, threads())
-    a_ref, _ = oracle.attention_rows(q2, k2, np.abs(v2), cu, scale, False, toks, heads, threads())
-    _, lse2 = oracle.attention_rows(q2, k2, v2, cu, 2 * scale, False, toks, heads, threads())
+    rows = lambda vv, sc: oracle.attention_rows_gqa(q2, k2, vv, cu, cu, sc, False, toks, heads,
+                                                     threads())
+    o_ref, lse_ref = rows(v2, scale)
+    a_ref, _ = rows(np.abs(v2), scale)
+    _, lse2 = rows(v2, 2 * scale)
     og = o.float().cpu().numpy()[0][toks, heads]
     lg = lse.cpu().numpy()[0][heads, toks]
     tol = o_tolerance(o_ref, a_ref, dtype, n_eff(lse_ref, lse2)[:, None])
     err = np.abs(og - o_ref)
-    print(f"split tail d={d} {dtype}: H={H}, {T} tiles, split from {first_split}: "
+    print(f"split tail d={d} {dtype} H/H_kv={grp}: H={H}, {T} tiles, split from {first_split}: "
           f"max |dO| {err.max():.3e}, max |dlse| {np.abs(lg - lse_ref).max():.3e}")
     assert np.all(err <= tol), float((err - tol).max())
     assert float(np.abs(lg - lse_ref).max()) <= TOL_LSE
