@@ -112,10 +112,10 @@ struct Cfg {
   static_assert(NS >= 3, "K/V ring too small");
   static_assert((NS & (NS - 1)) == 0, "K/V ring size must be a power of two");
   // K and V tiles alternate through the ring, so with an even ring a slot
-  // always holds K (consumed by the S issuer) or always V (the O issuer), and
-  // each full barrier has one waiter that sees its phases in order.  With an
-  // odd ring one issuer could reach a slot's next use while the other's use
-  // of it is still pending, and its parity wait would pass a phase early.
+  // always holds K or always V, and every issuer that waits on a slot's full
+  // barrier waits for each of its phases in order.  With an odd ring one
+  // issuer could reach a slot's next use while its other use was still
+  // pending, and its parity wait would pass a phase early.
   static_assert(NS % 2 == 0, "K/V ring size must be even");
   // MMA shapes.  Each instruction consumes 32 bytes of K per row.
   static constexpr int kKStep = 32 / kElt;             // 16 (16-bit) or 32 (e4m3)
@@ -298,10 +298,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
+    // dual issuers: both release the Q buffer and every K/V slot
+    mbar_init(bar_q_empty, C::kDual ? 2 : 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&bar_kv_full[i], 1);
-      mbar_init(&bar_kv_empty[i], 1);
+      mbar_init(&bar_kv_empty[i], C::kDual ? 2 : 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_full[x], 1);
@@ -475,55 +476,55 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       };
 
       if constexpr (C::kDual) {
-        // e4m3, and 16-bit at d = 64: two issuing threads.  Warp kWarpMMA
-        // issues S_X(j) = Q_X K_j^T as soon as softmax X has read S_X(j-1);
-        // warp kWarpPV issues O_X += P_X(j) V_j as soon as P_X(j) is written
-        // (shared memory for e4m3, its own TMEM columns for 16-bit).  Each
-        // commit covers only the committing thread's MMAs, so the barrier
-        // traffic of one issuer overlaps the other's tensor work.
-        const bool qk_role = warp == C::kWarpMMA;
+        // e4m3, and 16-bit at d = 64: one issuing thread per sub-tile.  Warp
+        // kWarpMMA serves sub-tile A, warp kWarpPV sub-tile B; each issues
+        // S_X(j+1) = Q_X K_{j+1}^T as soon as softmax X has read S_X(j), then
+        // O_X += P_X(j) V_j as soon as P_X(j) is written (shared memory for
+        // e4m3, its own TMEM columns for 16-bit), so neither sub-tile's
+        // products wait for the other's softmax.  Both issuers release every
+        // K/V slot and the Q buffer (two arrivals each); the one with fewer
+        // key tiles (A, on the causal diagonal) still waits for the copies
+        // of the tiles it skips, so it sees every slot's phases in order.
+        const int x = warp == C::kWarpMMA ? 0 : 1;
         for (int t = blockIdx.x; ok && get_tile<C>(p, t, num_tiles, ti); t += gridDim.x, ++tcount) {
-          const int nA = ti.nA, nB = ti.nB;
-          if (qk_role) {
-            if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            for (int j = 0; j < nB; ++j) {
-              const unsigned pk = kv_pos + 2 * j;
-              if (!wait_kv(pk)) { ok = false; break; }
-              if (j < nA) {
-                if (!wait_s_free(0)) { ok = false; break; }
-                issue_qk(0, pk);
-                mma_commit(&bar_s_full[0]);
-              }
-              if (!wait_s_free(1)) { ok = false; break; }
-              issue_qk(1, pk);
-              mma_commit(&bar_s_full[1]);
+          const int nX = x == 0 ? ti.nA : ti.nB, nB = ti.nB;
+          if (!mbar_wait(bar_q_full, tcount & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          // S_X(0)
+          if (!wait_kv(kv_pos) || !wait_s_free(x)) { ok = false; break; }
+          issue_qk(x, kv_pos);
+          mma_commit(&bar_s_full[x]);
+          mma_commit(&bar_kv_empty[kv_pos & (C::NS - 1)]);
+          if (nX == 1) mma_commit(bar_q_empty);
+          for (int j = 0; j < nX; ++j) {
+            if (j + 1 < nX) {   // S_X(j+1)
+              const unsigned pk = kv_pos + 2 * (j + 1);
+              if (!wait_kv(pk) || !wait_s_free(x)) { ok = false; break; }
+              issue_qk(x, pk);
+              mma_commit(&bar_s_full[x]);
               mma_commit(&bar_kv_empty[pk & (C::NS - 1)]);
-              if (j == nB - 1) mma_commit(bar_q_empty);
+              if (j + 2 == nX) mma_commit(bar_q_empty);
             }
-          } else {
-            for (int j = 0; j < nB; ++j) {
-              const unsigned pv = kv_pos + 2 * j + 1;
-              // the V tile and the previous tile's epilogue come first: they
-              // are usually ready long before P, which is then the only
-              // wait between the softmax's arrival and the MMAs
-              if (!wait_kv(pv)) { ok = false; break; }
-              if (j < nA) {
-                if (j == 0 && !mbar_wait(&bar_o_free[0], (tcount & 1) ^ 1, wc)) { ok = false; break; }
-                if (!wait_p(0)) { ok = false; break; }
-                if constexpr (C::kSmemP) issue_pv_smem(0, pv, j > 0);
-                else issue_pv(0, pv, j > 0);
-                mma_commit(&bar_o_done[0]);
-                if (j == nA - 1) mma_commit(&bar_o_final[0]);
-              }
-              if (j == 0 && !mbar_wait(&bar_o_free[1], (tcount & 1) ^ 1, wc)) { ok = false; break; }
-              if (!wait_p(1)) { ok = false; break; }
-              if constexpr (C::kSmemP) issue_pv_smem(1, pv, j > 0);
-              else issue_pv(1, pv, j > 0);
-              mma_commit(&bar_o_done[1]);
-              if (j == nB - 1) mma_commit(&bar_o_final[1]);
-              mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
+            // O_X (+)= P_X(j) V_j
+            const unsigned pv = kv_pos + 2 * j + 1;
+            if (!wait_kv(pv)) { ok = false; break; }
+            if (j == 0 && !mbar_wait(&bar_o_free[x], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+            if (!wait_p(x)) { ok = false; break; }
+            if constexpr (C::kSmemP) issue_pv_smem(x, pv, j > 0);
+            else issue_pv(x, pv, j > 0);
+            mma_commit(&bar_o_done[x]);
+            if (j == nX - 1) mma_commit(&bar_o_final[x]);
+            mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
+          }
+          if (!ok) break;
+          // key tiles of the other sub-tile only
+          for (int j = nX; j < nB; ++j) {
+            for (int u = 0; u < 2; ++u) {
+              const unsigned pos = kv_pos + 2 * j + u;
+              if (!wait_kv(pos)) { ok = false; break; }
+              mma_commit(&bar_kv_empty[pos & (C::NS - 1)]);
             }
+            if (!ok) break;
           }
           kv_pos += 2 * nB;
         }
