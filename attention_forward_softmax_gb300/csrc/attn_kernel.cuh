@@ -11,32 +11,32 @@
 // How it is laid out on the GPU (our design, not the card's Hopper one):
 //  * one CTA per SM, persistent over work tiles; a work tile is 256 query
 //    rows of one (sequence, head), split into two 128-row sub-tiles A and B;
-//  * warp roles, 16-bit (320 threads; 352 at d = 64):
+//  * warp roles, 16-bit at d = 128 (320 threads):
 //      warps 0-3  softmax warpgroup for sub-tile A (one thread per row)
 //      warps 4-7  softmax warpgroup for sub-tile B
-//      warp  8    MMA issuer (one thread) + TMEM allocation; at d = 64 only
-//                 S = Q K^T, P having its own TMEM columns there
+//      warp  8    MMA issuer (one thread) + TMEM allocation
 //      warp  9    TMA producer (one thread)
-//      warp 10    d = 64 only: O += P V issuer
-//  * warp roles, e4m3 (352 threads):
+//  * warp roles, e4m3 and 16-bit at d = 64 (352 threads), where S is free
+//    as soon as the softmax has read it:
 //      warps 0-7  softmax, one thread per row (sub-tile A, then B)
-//      warp  8    S = Q K^T issuer + TMEM allocation
+//      warp  8    MMA issuer of sub-tile A (S_A and O_A) + TMEM allocation
 //      warp  9    TMA producer
-//      warp 10    O += P V issuer
+//      warp 10    MMA issuer of sub-tile B
 //  * Q sub-tiles stay in shared memory for the whole tile; K and V tiles of
 //    128 keys stream through a ring of NS slots (K_0, V_0, K_1, V_1, ...);
 //  * TMEM (512 columns): S_A [0,128), S_B [128,256), O_A, O_B after them;
-//    16-bit P is written back over the first columns of its S; e4m3 P goes
-//    to one shared-memory tile per sub-tile;
-//  * 16-bit tensor-core order per key block j:  S_A(j), O_B += P_B(j-1)
+//    16-bit P is written back over the first columns of its S at d = 128
+//    and gets its own columns after O at d = 64; e4m3 P goes to one
+//    shared-memory tile per sub-tile;
+//  * 16-bit tensor-core order per key block j at d = 128:  S_A(j), O_B += P_B(j-1)
 //    V_{j-1}, S_B(j), O_A += P_A(j) V_j -- so each softmax warpgroup works
 //    while the tensor core serves the other sub-tile.  A commit after S_X(j)
 //    also covers the earlier O_X update, so when softmax X sees S_X(j) ready
 //    its O is current and it may rescale O in place;
-//  * e4m3: S_X(j+1) is issued as soon as softmax X has read S_X(j) into
-//    registers, by its own issuing thread; O_X += P_X(j) V_j waits for the P
-//    tile, and the softmax waits for that update before it rescales O_X or
-//    rewrites the tile;
+//  * e4m3 and d = 64: S_X(j+1) is issued as soon as softmax X has read
+//    S_X(j) into registers, by the issuing thread of sub-tile X;
+//    O_X += P_X(j) V_j waits for P, and the softmax waits for that update
+//    before it rescales O_X or rewrites P;
 //  * the output is rescaled only when a row max grows by more than
 //    kRescaleThresh (log2 units); otherwise the stale max is kept, which is
 //    exact after the final division by l;
@@ -146,12 +146,12 @@ struct Cfg {
   // as in the e4m3 path (P in TMEM rather than shared memory).
   static constexpr bool kSepP = !kFp8 && D == 64;
   static constexpr uint32_t kColP0 = 256 + 2 * D;        // kSepP: P_X at kColP0 + 64 x
-  static constexpr bool kDual = kSmemP || kSepP;         // separate S and O issuers
+  static constexpr bool kDual = kSmemP || kSepP;         // one MMA issuer per sub-tile
   // softmax warps: one thread per query row of the two sub-tiles
   static constexpr int kSoftmaxWarps = 8;
-  static constexpr int kWarpMMA = kSoftmaxWarps;       // MMA issuer (S = Q K^T) + TMEM allocation
+  static constexpr int kWarpMMA = kSoftmaxWarps;       // MMA issuer (kDual: of sub-tile A) + TMEM allocation
   static constexpr int kWarpTMA = kSoftmaxWarps + 1;   // TMA producer
-  static constexpr int kWarpPV = kSoftmaxWarps + 2;    // e4m3: second issuer (O += P V)
+  static constexpr int kWarpPV = kSoftmaxWarps + 2;    // kDual: MMA issuer of sub-tile B
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 2 + (kDual ? 1 : 0));
   // arrivals per phase on the barriers the softmax signals: one per softmax
   // thread of the sub-tile
