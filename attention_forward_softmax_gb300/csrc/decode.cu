@@ -16,11 +16,16 @@
 // Design.  Decoding is bound by HBM: each key brings 4 d bytes of K and V
 // and meets only the R = (H / H_kv) * Nq query rows of its K/V head.  So one
 // CTA takes one (sequence, K/V head, key range) and streams that range once:
-//  * 64-key tiles of K and V are gathered row by row through the page table
-//    with 16-byte cp.async copies into XOR-swizzled shared-memory tiles, two
-//    stages per CTA and three CTAs per SM, so the next tile's rows are in
-//    flight while this one is used (measured: more CTAs per SM beat deeper
-//    stages in fewer CTAs);
+//  * 64-key tiles of K and V arrive through the page table, two stages per
+//    CTA and three CTAs per SM, so the next tile is in flight while this one
+//    is used (measured: more CTAs per SM beat deeper stages in fewer CTAs).
+//    When a page splits into pieces of 16, 32 or 64 rows, one thread copies
+//    each piece with a tensor copy (a box of those rows and 64 columns of
+//    the cache seen as a (d, H_kv, pages * page_size) tensor, 128-byte
+//    swizzle) completing on the stage's mbarrier; other page sizes gather
+//    rows with 16-byte cp.async copies into XOR-swizzled tiles.  The
+//    mbarrier waits are bounded: on expiry the CTA records ATTN_ERR_TIMEOUT,
+//    lets its copies land and returns;
 //  * the key range of a sequence is cut into chunks of equal size, one per
 //    CTA, so long and short sequences spread evenly over the SMs;
 //  * the R <= 16 query rows are one 16-row MMA tile; each of the four warps
@@ -59,8 +64,11 @@ struct DecodeArgs {
   int B, Nq, H, Hkv, page_size, max_pages, num_pages;
   int splits;                      // CTAs per (sequence, K/V head): ceil(max_seqlen_k / chunk)
   int chunk;                       // keys per CTA (a multiple of kTileKeys)
+  int box_rows;                    // tensor-copy path: cache rows per copy (16, 32 or 64)
   float scale_log2;
   int causal;
+  int *status;                     // device status word
+  long long budget;                // clock64 cycles per pipeline wait
 };
 
 template <int D>
@@ -68,8 +76,8 @@ struct DecSmem {
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kTileKeys * kRowBytes;     // one K or V tile
   static constexpr int kOffQ = 0;                              // 16 rows
-  static constexpr int kOffKV = kRows * kRowBytes;             // [stage][K, V]
-  static constexpr int kBytes = kOffKV + kStages * 2 * kTileBytes;
+  static constexpr int kOffKV = kRows * kRowBytes;             // [stage][K, V], 1024-aligned
+  static constexpr int kBytes = kOffKV + kStages * 2 * kTileBytes + 1024;   // + alignment slack
   // after the key loop the K/V area holds the warps' partial results
   static_assert(4 * kRows * (D + 2) * 4 <= kStages * 2 * kTileBytes, "merge area too small");
 };
@@ -80,6 +88,17 @@ struct DecSmem {
 template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return r * (D * 2) + ((c ^ (r & 7)) << 4);
+}
+
+// The same for a K or V tile: row-gathered tiles use swz; tiles written by
+// tensor copies hold D / 64 column blocks of 64 rows x 128 bytes, each with
+// the copy's 128-byte swizzle (16-byte unit u of row r at u ^ (r mod 8)).
+template <int D, bool kTma>
+__device__ __forceinline__ uint32_t kv_swz(int r, int c) {
+  if constexpr (kTma)
+    return (c >> 3) * (kTileKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  else
+    return swz<D>(r, c);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
@@ -124,14 +143,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kTma>
 __global__ void __launch_bounds__(kDecThreads)
-    decode_kernel(const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeArgs a) {
   using L = DecSmem<D>;
   constexpr int kChunks = D / 8;           // 16-byte chunks per row
   constexpr int kNT = D / 8;               // 8-column output tiles
-  extern __shared__ __align__(128) uint8_t dsm[];
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *dsm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(dsm);
+  __shared__ uint64_t full[kStages];       // tensor-copy path: a stage's copies landed
+  __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int g = a.H / a.Hkv;               // query heads per K/V head
@@ -145,6 +169,17 @@ __global__ void __launch_bounds__(kDecThreads)
   const size_t row_stride = static_cast<size_t>(a.Hkv) * D;   // elements between cache rows
   const uint16_t *kc = static_cast<const uint16_t *>(a.k);
   const uint16_t *vc = static_cast<const uint16_t *>(a.v);
+  if constexpr (kTma) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+      abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    __syncthreads();
+  }
+  const WaitCtl wc{&abort_flag, a.status, a.budget};
 
   // query rows r = qi * g + gh (query qi, head hk * g + gh) -> shared memory
   {
@@ -157,6 +192,29 @@ __global__ void __launch_bounds__(kDecThreads)
       cp_async16(sbase + L::kOffQ + swz<D>(r, c), src, r < R ? 16 : 0);
     }
   }
+  // one tile of K and V by tensor copies (one thread): a copy per box_rows
+  // cache rows (they lie in one page) and 64 columns; copies that would
+  // start at or past the end of the range are left out
+  auto issue_tile = [&](int tile, int stage) {
+    uint8_t *kdst = dsm + L::kOffKV + stage * 2 * L::kTileBytes;
+    uint8_t *vdst = kdst + L::kTileBytes;
+    const int br = a.box_rows;
+    int pieces = 0;
+    for (int pc = 0; pc < kTileKeys / br; ++pc)
+      if (tile * kTileKeys + pc * br < k1) ++pieces;
+    mbar_arrive_expect_tx(&full[stage], pieces * br * D * 2 * 2);
+    for (int pc = 0; pc < pieces; ++pc) {
+      const int t = tile * kTileKeys + pc * br;
+      const int page = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + t / a.page_size);
+      const int row = page * a.page_size + t % a.page_size;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int off = c * (kTileKeys * 128) + pc * br * 128;
+        tma_load_3d(kdst + off, &tmK, &full[stage], c * 64, hk, row);
+        tma_load_3d(vdst + off, &tmV, &full[stage], c * 64, hk, row);
+      }
+    }
+  };
   // gather one tile of K and V through the page table
   auto load_tile = [&](int tile, int stage) {
     const uint32_t kdst = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
@@ -186,28 +244,60 @@ __global__ void __launch_bounds__(kDecThreads)
   const int lim_a = a.causal ? Lk - a.Nq + ra / g : Lk - 1;
   const int lim_b = a.causal ? Lk - a.Nq + rb / g : Lk - 1;
 
-  // prologue: the first kStages - 1 tiles (one commit group per tile, empty
-  // groups included, so the group count per tile stays fixed)
+  // prologue: the first kStages - 1 tiles (row gathers: one commit group per
+  // tile, empty groups included, so the group count per tile stays fixed)
+  if constexpr (kTma) {
+    if (threadIdx.x == 0)
+      for (int i = 0; i < kStages - 1; ++i)
+        if (t0 + i < t1) issue_tile(t0 + i, i);
+    cp_async_commit();                     // the Q rows
+  } else {
 #pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (t0 + i < t1) load_tile(t0 + i, i);
-    cp_async_commit();
+    for (int i = 0; i < kStages - 1; ++i) {
+      if (t0 + i < t1) load_tile(t0 + i, i);
+      cp_async_commit();
+    }
   }
   uint32_t qf[D / 16][4];                  // Q fragments, loaded once
-  for (int tile = t0; tile < t1; ++tile) {
+  bool ok = true;
+  int tile = t0;
+  for (; tile < t1; ++tile) {
     const int stage = (tile - t0) % kStages;
-    // refill the stage read one iteration ago (freed by its closing barrier)
-    if (tile + kStages - 1 < t1) load_tile(tile + kStages - 1, (tile - t0 + kStages - 1) % kStages);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
+    const int nxt = tile + kStages - 1, nstage = (tile - t0 + kStages - 1) % kStages;
+    if constexpr (kTma) {
+      // refill the stage read one iteration ago (freed by its closing
+      // barrier; its generic reads ordered before the copy)
+      if (threadIdx.x == 0 && nxt < t1) {
+        fence_proxy_async_smem();
+        issue_tile(nxt, nstage);
+      }
+      if (tile == t0) cp_async_wait<0>();
+      const bool got = mbar_wait(&full[stage], ((tile - t0) / kStages) & 1, wc);
+      if (!__syncthreads_and(got)) { ok = false; break; }
+    } else {
+      // refill the stage read one iteration ago (freed by its closing barrier)
+      if (nxt < t1) load_tile(nxt, nstage);
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();
+      __syncthreads();
+    }
+    const uint32_t kt = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
+    const uint32_t vt = kt + L::kTileBytes;
+    if (kTma && tile * kTileKeys + kTileKeys > k1) {
+      // keys at or past the end of the range: their V rows may hold another
+      // tile's values or rows of the page past the sequence; zero them (P is
+      // 0 there, and 0 * V must be 0)
+      const int r0 = max(0, k1 - tile * kTileKeys);
+      for (int id = threadIdx.x; id < (kTileKeys - r0) * kChunks; id += kDecThreads)
+        st_shared_v4(vt + kv_swz<D, kTma>(r0 + id / kChunks, id % kChunks), 0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();            // before a later copy into this stage
+      __syncthreads();
+    }
     if (tile == t0) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         ldsm_x4(sbase + L::kOffQ + swz<D>(lane & 15, 2 * ks + (lane >> 4)), qf[ks]);
     }
-    const uint32_t kt = sbase + L::kOffKV + stage * 2 * L::kTileBytes;
-    const uint32_t vt = kt + L::kTileBytes;
     const int kw = warp * 16;              // this warp's keys within the tile
     // S = Q K^T for 16 keys: two 8-key tiles (one ldmatrix per k step)
     float s[2][4];
@@ -217,7 +307,7 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t kb[4];
       const int key = kw + (lane & 7) + ((lane >> 4) << 3);
-      ldsm_x4(kt + swz<D>(key, 2 * ks + ((lane >> 3) & 1)), kb);
+      ldsm_x4(kt + kv_swz<D, kTma>(key, 2 * ks + ((lane >> 3) & 1)), kb);
       mma16816<BF16>(s[0], qf[ks], kb[0], kb[1]);
       mma16816<BF16>(s[1], qf[ks], kb[2], kb[3]);
     }
@@ -274,13 +364,20 @@ __global__ void __launch_bounds__(kDecThreads)
       for (int np = 0; np < kNT / 2; ++np) {
         uint32_t vb[4];
         const int key = kw + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        ldsm_x4_t(vt + swz<D>(key, 2 * np + (lane >> 4)), vb);
+        ldsm_x4_t(vt + kv_swz<D, kTma>(key, 2 * np + (lane >> 4)), vb);
         mma16816<BF16>(o[2 * np], pf[ks], vb[0], vb[1]);
         mma16816<BF16>(o[2 * np + 1], pf[ks], vb[2], vb[3]);
       }
     __syncthreads();                       // this stage may be refilled next
   }
   cp_async_wait<0>();
+  if (!ok) {
+    // a wait gave up: let the copies still in flight land, then leave
+    if (kTma && threadIdx.x == 0)
+      for (int u = tile; u < tile + kStages && u < t1; ++u)   // issued: up to tile + kStages - 1
+        mbar_wait_drain(&full[(u - t0) % kStages], ((u - t0) / kStages) & 1);
+    return;
+  }
   __syncthreads();
 
   // merge the four warps' partial results through shared memory
@@ -392,20 +489,20 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
   if (lane == 0 && a.lse != nullptr) a.lse[row] = z > 0.f ? mx + logf(z) : -INFINITY;
 }
 
-template <int D, bool BF16>
-attn_status_t launch_decode(DecodeArgs &a, int num_sms, cudaStream_t s) {
+template <int D, bool BF16, bool kTma>
+attn_status_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, DecodeArgs &a,
+                            cudaStream_t s) {
   using L = DecSmem<D>;
   static std::once_flag once[kMaxDevices];
   static cudaError_t err[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   std::call_once(once[dev], [dev] {
-    err[dev] = cudaFuncSetAttribute(decode_kernel<D, BF16>,
+    err[dev] = cudaFuncSetAttribute(decode_kernel<D, BF16, kTma>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   });
   if (err[dev] != cudaSuccess) return ATTN_ERR_LAUNCH;
-  (void)num_sms;
-  decode_kernel<D, BF16><<<dim3(a.splits, a.Hkv, a.B), kDecThreads, L::kBytes, s>>>(a);
+  decode_kernel<D, BF16, kTma><<<dim3(a.splits, a.Hkv, a.B), kDecThreads, L::kBytes, s>>>(mk, mv, a);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (a.splits > 1) {
     const int rows = a.B * a.H * a.Nq;
@@ -413,6 +510,13 @@ attn_status_t launch_decode(DecodeArgs &a, int num_sms, cudaStream_t s) {
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   }
   return ATTN_OK;
+}
+
+template <int D, bool BF16>
+attn_status_t launch_decode_any(const CUtensorMap &mk, const CUtensorMap &mv, DecodeArgs &a,
+                                cudaStream_t s) {
+  return a.box_rows > 0 ? launch_decode<D, BF16, true>(mk, mv, a, s)
+                        : launch_decode<D, BF16, false>(mk, mv, a, s);
 }
 
 }  // namespace
@@ -480,10 +584,36 @@ extern "C" attn_status_t attn_fwd_paged(const void *q, const void *k_cache, cons
     a.ws_o = ds->split_ws;
     a.ws_lse = ds->split_ws + rows * splits * d;
   }
+  a.status = ds->status;
+  a.budget = wait_budget();
+  // Tensor copies of the cache when a page splits into copies of 16, 32 or
+  // 64 rows (64 % rows == 0 and page_size % rows == 0, so a tile's copies
+  // never cross a page): the cache as a (d, H_kv, num_pages * page_size)
+  // tensor, boxes of (64, 1, rows) with the 128-byte swizzle.  Otherwise the
+  // rows are gathered with 16-byte copies.
+  CUtensorMap mk{}, mv{};
+  {
+    int br = 64;
+    while (br >= 16 && page_size % br != 0) br >>= 1;
+    const long long rows = static_cast<long long>(num_pages) * page_size;
+    a.box_rows = (br >= 16 && rows < (1LL << 31)) ? br : 0;
+    if (a.box_rows > 0) {
+      const CUtensorMapDataType dt =
+          dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H_kv, (cuuint64_t)rows};
+      const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H_kv * d * 2};
+      const cuuint32_t box[3] = {64, 1, (cuuint32_t)a.box_rows};
+      if ((st = encode_tiled(&mk, dt, 3, k_cache, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK ||
+          (st = encode_tiled(&mv, dt, 3, v_cache, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B)) != ATTN_OK)
+        return st;
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128)
-    return dtype == ATTN_BF16 ? launch_decode<128, true>(a, ds->num_sms, s)
-                              : launch_decode<128, false>(a, ds->num_sms, s);
-  return dtype == ATTN_BF16 ? launch_decode<64, true>(a, ds->num_sms, s)
-                            : launch_decode<64, false>(a, ds->num_sms, s);
+    return dtype == ATTN_BF16 ? launch_decode_any<128, true>(mk, mv, a, s)
+                              : launch_decode_any<128, false>(mk, mv, a, s);
+  return dtype == ATTN_BF16 ? launch_decode_any<64, true>(mk, mv, a, s)
+                            : launch_decode_any<64, false>(mk, mv, a, s);
 }

@@ -221,7 +221,10 @@ attn_status_t attn_fwd_varlen_noalloc(const void *q, const void *k, const void *
  *                  per-device workspace the library allocates on first use
  *                  and grows when needed.
  * Limits: d = 64 or 128; (H / H_kv) * Nq <= 16 (ATTN_ERR_UNSUPPORTED
- * otherwise); any page_size >= 1.
+ * otherwise); any page_size >= 1.  Page sizes that split into pieces of 16,
+ * 32 or 64 rows are loaded by tensor copies whose waits are bounded: a wait
+ * past its budget records ATTN_ERR_TIMEOUT in the status word
+ * (attn_get_status) and the output is then undefined.
  */
 attn_status_t attn_fwd_paged(const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_table, const int32_t *seqlens_k, void *o,

@@ -72,7 +72,7 @@ def test_paged_decode_parity(d, causal, splits):
     check(6000 + d, [1, 300, 777, 129, 2048], 1, 8, 2, d, 16, causal, splits)
 
 
-@pytest.mark.parametrize("page_size", [1, 7, 64, 256])
+@pytest.mark.parametrize("page_size", [1, 7, 16, 48, 64, 96, 256])
 def test_paged_page_sizes(page_size):
     check(6100 + page_size, [513, 64, 1000], 2, 4, 1, 128, page_size, True, 0)
 
