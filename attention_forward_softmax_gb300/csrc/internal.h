@@ -62,12 +62,15 @@ struct DeviceState {
   size_t bwd_ws_bytes = 0;
   float *fwd_split_ws = nullptr;  // forward: partials of the split last tiles
   size_t fwd_split_ws_bytes = 0;
-  // host-buffer forward (attn_fwd_host): two device staging sets, the copy
-  // streams and the events that order copies and compute
+  // host-buffer forward (attn_fwd_host): kHostSets device staging sets, the
+  // copy streams, a second compute stream and the events that order copies
+  // and compute
+  static constexpr int kHostSets = 3;
   float *host_ws = nullptr;
   size_t host_ws_bytes = 0;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp2 = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSets] = {}, ev_comp[kHostSets] = {},
+              ev_out[kHostSets] = {};
   int num_sms = 0;
 };
 attn_status_t device_state(DeviceState **out);

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -228,9 +229,12 @@ using namespace attn;
 
 extern "C" {
 
-attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
-                           int B, int H, int H_kv, int N, int d, float scale, int causal,
-                           attn_dtype_t dtype, void *stream) {
+// The dense 16-bit forward; allow_split = false keeps the last wave whole
+// (no use of the per-device split workspace, so two such launches may run
+// at once on different streams).
+static attn_status_t fwd_dense(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int H, int H_kv, int N, int d, float scale, int causal,
+                               attn_dtype_t dtype, bool allow_split, cudaStream_t s) {
   attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
   if (st != ATTN_OK) return st;
   if (B < 1 || N < 1 || H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
@@ -247,9 +251,15 @@ attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o,
   a.scale = scale; a.causal = causal ? 1 : 0;
   a.num_tiles = static_cast<int>(tiles);
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
-  if ((st = plan_tail_split(ds, a)) != ATTN_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (allow_split && (st = plan_tail_split(ds, a)) != ATTN_OK) return st;
   return dtype == ATTN_BF16 ? launch_attn_bf16(a, false, s) : launch_attn_f16(a, false, s);
+}
+
+attn_status_t attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int H_kv, int N, int d, float scale, int causal,
+                           attn_dtype_t dtype, void *stream) {
+  return fwd_dense(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, dtype, true,
+                   static_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_fwd_bias(const void *q, const void *k, const void *v, const float *bias,
@@ -296,28 +306,53 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
   if (st != ATTN_OK) return st;
   if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
-  const size_t per_b = static_cast<size_t>(N) * H * d * 2;        // q, k, v or o of one entry
-  const size_t lse_b = static_cast<size_t>(H) * N * sizeof(float);
   if (static_cast<long long>(N) * H * d > (1LL << 40) / B) return ATTN_ERR_TOO_LARGE;
-  // one staging set: q, k, v, o and lse of one batch entry, 256-byte aligned parts
+  constexpr int S = DeviceState::kHostSets;
+  const size_t row = static_cast<size_t>(H) * d * 2;            // one token of q, k, v or o
+  const size_t per_b = static_cast<size_t>(N) * row;            // one batch entry
+  const size_t lse_b = static_cast<size_t>(H) * N * sizeof(float);
+  // one staging set: q, k, v, o and lse of up to one batch entry, 256-byte
+  // aligned parts
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t set_bytes = 4 * up(per_b) + up(lse_b);
   DeviceState *ds = nullptr;
   if ((st = device_state(&ds)) != ATTN_OK) return st;
-  if ((st = grow_workspace(&ds->host_ws, &ds->host_ws_bytes, 2 * set_bytes)) != ATTN_OK) return st;
+  if ((st = grow_workspace(&ds->host_ws, &ds->host_ws_bytes, S * set_bytes)) != ATTN_OK) return st;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (ds->h2d == nullptr) {
       if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
           cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&ds->comp2, cudaStreamNonBlocking) != cudaSuccess ||
           cudaEventCreateWithFlags(&ds->ev_start, cudaEventDisableTiming) != cudaSuccess)
         return ATTN_ERR_CUDA;
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < S; ++i)
         if (cudaEventCreateWithFlags(&ds->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ds->ev_comp[i], cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ds->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
           return ATTN_ERR_CUDA;
     }
+  }
+  // Work items ("chunks"): whole batch entries, except that the first and
+  // the last entry are cut into groups of hg heads -- the fewest heads whose
+  // 256-row tiles still fill every SM once -- so the compute starts after a
+  // smaller first copy and what is left after the last copy is short.  A
+  // chunk's rows are strided in the host arrays (hg of H heads per token):
+  // 2-D copies move them to and from compact staging buffers.
+  const int nqt = (N + 255) / 256;
+  int hg = H;
+  for (int x = 1; x < H; ++x)
+    if (H % x == 0 && static_cast<long long>(x) * nqt >= ds->num_sms) {
+      hg = x;
+      break;
+    }
+  struct Chunk { int b, h0, nh; };
+  std::vector<Chunk> chunks;
+  for (int b = 0; b < B; ++b) {
+    if ((b == 0 || b == B - 1) && hg < H)
+      for (int h0 = 0; h0 < H; h0 += hg) chunks.push_back({b, h0, hg});
+    else
+      chunks.push_back({b, 0, H});
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const char *qh = static_cast<const char *>(q), *kh = static_cast<const char *>(k);
@@ -329,37 +364,48 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
   // everything queued on the caller's stream before this call comes first
   chk(cudaEventRecord(ds->ev_start, s));
   chk(cudaStreamWaitEvent(ds->h2d, ds->ev_start, 0));
-  for (int c = 0; ok && c < B; ++c) {
-    const int set = c & 1;
+  const int nc = static_cast<int>(chunks.size());
+  int last_set = 0;
+  for (int c = 0; ok && c < nc; ++c) {
+    const Chunk ch = chunks[c];
+    const int set = c % S;
+    last_set = set;
     char *dq = ws + set * set_bytes, *dk = dq + up(per_b), *dv = dk + up(per_b);
     char *dout = dv + up(per_b);
     float *dlse = reinterpret_cast<float *>(dout + up(per_b));
-    // inputs of entry c, once entry c - 2 (same set) has been computed (one
-    // copy stream: a second one measured slower, the two share the host link)
-    if (c >= 2) chk(cudaStreamWaitEvent(ds->h2d, ds->ev_comp[set], 0));
-    chk(cudaMemcpyAsync(dq, qh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
-    chk(cudaMemcpyAsync(dk, kh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
-    chk(cudaMemcpyAsync(dv, vh + c * per_b, per_b, cudaMemcpyHostToDevice, ds->h2d));
+    const size_t w = static_cast<size_t>(ch.nh) * d * 2;        // bytes of a chunk row
+    const size_t hoff = static_cast<size_t>(ch.b) * per_b + static_cast<size_t>(ch.h0) * d * 2;
+    // inputs, once chunk c - S (same set) has been computed (one copy
+    // stream: a second one measured slower, the two share the host link)
+    if (c >= S) chk(cudaStreamWaitEvent(ds->h2d, ds->ev_comp[set], 0));
+    chk(cudaMemcpy2DAsync(dq, w, qh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpy2DAsync(dk, w, kh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpy2DAsync(dv, w, vh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
     chk(cudaEventRecord(ds->ev_in[set], ds->h2d));
-    // compute on the caller's stream, once the inputs are in and entry c - 2's
-    // outputs have left the set
-    chk(cudaStreamWaitEvent(s, ds->ev_in[set], 0));
-    if (c >= 2) chk(cudaStreamWaitEvent(s, ds->ev_out[set], 0));
+    // compute on the caller's stream and the second compute stream in turn
+    // (one chunk's last wave overlaps the next chunk's first), once the
+    // inputs are in and chunk c - S's outputs have left the set
+    cudaStream_t cs = (c & 1) ? ds->comp2 : s;
+    chk(cudaStreamWaitEvent(cs, ds->ev_in[set], 0));
+    if (c >= S) chk(cudaStreamWaitEvent(cs, ds->ev_out[set], 0));
     if (!ok) break;
-    if ((st = attn_fwd_gqa(dq, dk, dv, dout, lse ? dlse : nullptr, 1, H, H, N, d, scale, causal,
-                           dtype, stream)) != ATTN_OK)
+    if ((st = fwd_dense(dq, dk, dv, dout, lse ? dlse : nullptr, 1, ch.nh, ch.nh, N, d, scale,
+                        causal, dtype, false, cs)) != ATTN_OK)
       return st;
-    chk(cudaEventRecord(ds->ev_comp[set], s));
-    // outputs of entry c
+    chk(cudaEventRecord(ds->ev_comp[set], cs));
+    // outputs of the chunk
     chk(cudaStreamWaitEvent(ds->d2h, ds->ev_comp[set], 0));
-    chk(cudaMemcpyAsync(oh + c * per_b, dout, per_b, cudaMemcpyDeviceToHost, ds->d2h));
-    if (lse) chk(cudaMemcpyAsync(lse + static_cast<size_t>(c) * H * N, dlse, lse_b,
-                                 cudaMemcpyDeviceToHost, ds->d2h));
+    chk(cudaMemcpy2DAsync(oh + hoff, row, dout, w, w, N, cudaMemcpyDeviceToHost, ds->d2h));
+    if (lse)
+      chk(cudaMemcpyAsync(lse + (static_cast<size_t>(ch.b) * H + ch.h0) * N, dlse,
+                          static_cast<size_t>(ch.nh) * N * sizeof(float), cudaMemcpyDeviceToHost,
+                          ds->d2h));
     chk(cudaEventRecord(ds->ev_out[set], ds->d2h));
   }
   // later work on the caller's stream sees the outputs (the copy-out stream
-  // runs in order, so its last event covers every entry)
-  if (ok) chk(cudaStreamWaitEvent(s, ds->ev_out[(B - 1) & 1], 0));
+  // runs in order and every copy-out follows its chunk's compute, so its
+  // last event covers both compute streams)
+  if (ok) chk(cudaStreamWaitEvent(s, ds->ev_out[last_set], 0));
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -470,7 +516,7 @@ void attn_shutdown(void) {
     if (ds.bwd_ws) cudaFree(ds.bwd_ws);
     if (ds.fwd_split_ws) cudaFree(ds.fwd_split_ws);
     if (ds.host_ws) cudaFree(ds.host_ws);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < DeviceState::kHostSets; ++i) {
       if (ds.ev_in[i]) cudaEventDestroy(ds.ev_in[i]);
       if (ds.ev_comp[i]) cudaEventDestroy(ds.ev_comp[i]);
       if (ds.ev_out[i]) cudaEventDestroy(ds.ev_out[i]);
@@ -478,6 +524,7 @@ void attn_shutdown(void) {
     if (ds.ev_start) cudaEventDestroy(ds.ev_start);
     if (ds.h2d) cudaStreamDestroy(ds.h2d);
     if (ds.d2h) cudaStreamDestroy(ds.d2h);
+    if (ds.comp2) cudaStreamDestroy(ds.comp2);
     if (ds.status) cudaFree(ds.status);
     ds = DeviceState{};
   }

@@ -83,15 +83,18 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
 /*
  * attn_fwd with HOST buffers: the same dense forward for data that lives in
  * host memory (q, k, v, o, lse as in attn_fwd, but host pointers; H_kv = H).
- * The library copies one batch entry at a time to the device while the
- * previous entry is computed and the one before it copied back: two device
- * staging sets in the per-device workspace, two internal copy streams (in
- * and out) and events.  The compute runs on `stream`, and `stream` waits for the last
- * copy back, so later work on it sees the outputs; the host buffers must
- * stay valid until then.  Use page-locked host memory (cudaHostAlloc or
- * cudaHostRegister): copies from pageable memory are correct but do not
- * overlap.  B = 1 gives no overlap.  Errors as attn_fwd, plus ATTN_ERR_CUDA
- * when a copy or event call fails.
+ * The library moves the work in chunks -- whole batch entries, and for the
+ * first and the last entry groups of heads (the fewest heads whose work
+ * tiles still fill every SM once) -- copying one chunk in while earlier
+ * chunks are computed and copied back: three device staging sets in the
+ * per-device workspace, internal copy-in, copy-out and second compute
+ * streams, and events.  The compute runs on `stream` and the second compute
+ * stream in turn, without the split last wave (each tile computed whole),
+ * and `stream` waits for the last copy back, so later work on it sees the
+ * outputs; the host buffers must stay valid until then.  Use page-locked
+ * host memory (cudaHostAlloc or cudaHostRegister): copies from pageable
+ * memory are correct but do not overlap.  Errors as attn_fwd, plus
+ * ATTN_ERR_CUDA when a copy or event call fails.
  */
 attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
                             int B, int H, int N, int d, float scale, int causal,

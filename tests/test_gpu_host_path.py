@@ -1,10 +1,12 @@
-"""attn_fwd_host: the dense forward on host buffers, copies of one batch
-entry overlapped with the compute of the previous one.  It runs the same
-kernel on each batch entry that attn_fwd runs on the whole batch, and at
-these sizes (fewer work tiles than SMs, so no tile is split) every tile is
+"""attn_fwd_host: the dense forward on host buffers, copies of one chunk
+(a batch entry, or a group of heads of the first and last entries)
+overlapped with the compute of earlier chunks.  It runs the same kernel on
+each chunk that attn_fwd runs on the whole batch, without splitting the last
+wave; at shapes where attn_fwd splits nothing either, every tile is
 computed the same way: the outputs must be bitwise equal to attn_fwd's on
-device copies of the same inputs.  Also: pageable host memory, no lse,
-B = 1, and stream order (work queued after the call sees the outputs)."""
+device copies of the same inputs.  Also: head-group chunks, pageable host
+memory, no lse, B = 1, and stream order (work queued after the call sees
+the outputs)."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +36,34 @@ def device_reference(q, k, v, causal):
 ])
 def test_host_path_matches_device_path_bitwise(B, N, H, d, dtype, causal):
     q, k, v = qkv(9500 + N, (B, N, H, d), dtype)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o, lse = agb.attn_fwd_host(hq, hk, hv, causal=causal)
+    torch.cuda.current_stream().synchronize()
+    assert agb.get_status() == 0
+    o_ref, lse_ref = device_reference(q, k, v, causal)
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
+
+
+def no_split(B, H, N):
+    """attn_fwd leaves every tile whole at this shape (non-causal)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = B * H * ((N + 255) // 256)
+    grid = min(T, sms)
+    rem = T % grid
+    return rem == 0 or 2 * rem > grid
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(2, 32, 4096, False), (3, 48, 4096, True)])
+def test_host_path_head_group_chunks(B, H, N, causal):
+    """Shapes whose 256-row tiles fill the SMs with fewer heads than H, so
+    the first and last entries move as head groups (strided 2-D copies)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nqt = (N + 255) // 256
+    assert any(H % x == 0 and x * nqt >= sms for x in range(1, H)), "no head groups here"
+    if not causal and not no_split(B, H, N):
+        pytest.skip("attn_fwd would split the last wave at this SM count")
+    q, k, v = qkv(9530 + H, (B, N, H, 128), torch.bfloat16)
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     o, lse = agb.attn_fwd_host(hq, hk, hv, causal=causal)
     torch.cuda.current_stream().synchronize()
