@@ -29,8 +29,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           6: "ATTN_ERR_BAD_SEQLENS", 7: "ATTN_ERR_CUDA", 8: "ATTN_ERR_TOO_LARGE"}
 EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_fp8", "qkv_block_quant_hadamard",
            "attn_get_status", "attn_fwd_varlen_noalloc", "attn_fwd_gqa", "attn_fwd_varlen_gqa",
-           "attn_fwd_paged", "attn_fwd_bias", "attn_bwd", "attn_fwd_host", "attn_status_string",
-           "attn_shutdown", "attn_version")
+           "attn_fwd_paged", "attn_fwd_bias", "attn_bwd", "attn_fwd_host", "attn_fwd_fp8_host",
+           "attn_status_string", "attn_shutdown", "attn_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -78,7 +78,8 @@ def lib() -> ctypes.CDLL:
                                         vp]
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
             L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
-            for nm in EXPORTS[:12]:
+            L.attn_fwd_fp8_host.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+            for nm in EXPORTS[:13]:
                 getattr(L, nm).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -246,8 +247,9 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out
                   lse=None, want_lse: bool = True, stream=None):
     """attn_fwd on HOST tensors q, k, v [B, N, H, d] (bf16/fp16, contiguous,
     page-locked for overlap) -> host (o, lse); the library pipelines the
-    copies with the compute one batch entry at a time.  The call is
-    asynchronous on `stream`: synchronise it before reading o and lse."""
+    copies with the compute in chunks (batch entries, head groups of the
+    first and last entry).  The call is asynchronous on `stream`:
+    synchronise it before reading o and lse."""
     for t in (q, k, v, out, lse):
         if t is not None and (t.is_cuda or not t.is_contiguous()):
             raise ValueError("attn_fwd_host takes contiguous host tensors")
@@ -260,6 +262,32 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out
     rc = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
                              int(bool(causal)), _dtype_code(q), _stream(stream))
     _check(rc, "attn_fwd_host")
+    return o, lse
+
+
+def attn_fwd_fp8_host(q, k, v, signs=None, causal: bool = False, scale: float | None = None,
+                      out=None, lse=None, want_lse: bool = True, stream=None):
+    """The 8-bit path on HOST tensors: bf16 q, k, v [B, N, H, d] (contiguous,
+    page-locked for overlap), optional int8 signs [d] (host) -> host bf16 o
+    and fp32 lse; block quantisation (with the rotation when signs are
+    given) and the e4m3 forward run on the device per chunk, pipelined with
+    the copies.  Asynchronous on `stream`: synchronise it before reading."""
+    for t in (q, k, v, signs, out, lse):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("attn_fwd_fp8_host takes contiguous host tensors")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("attn_fwd_fp8_host takes bf16 q, k, v")
+    if signs is not None and (signs.dtype != torch.int8 or signs.numel() != q.shape[-1]):
+        raise ValueError("signs must be int8 of length d")
+    B, N, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    pin = q.is_pinned()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    rc = lib().attn_fwd_fp8_host(_ptr(q), _ptr(k), _ptr(v), _ptr(signs), _ptr(o), _ptr(lse), B,
+                                 H, N, d, scale, int(bool(causal)), _stream(stream))
+    _check(rc, "attn_fwd_fp8_host")
     return o, lse
 
 

@@ -222,6 +222,122 @@ attn_status_t check_common(const void *q, const void *k, const void *v, const vo
   return ATTN_OK;
 }
 
+// A piece of the work of a host-buffer forward: heads h0 .. h0 + nh - 1 of
+// batch entry b.
+struct HostChunk {
+  int b, h0, nh;
+};
+
+// Host-buffer pipeline of attn_fwd_host and attn_fwd_fp8_host.  The work is
+// cut into chunks: whole batch entries, except that the first and the last
+// entry are cut into groups of hg heads -- the fewest heads whose 256-row
+// tiles still fill every SM once -- so the compute starts after a smaller
+// first copy and little is left after the last one.  A chunk's rows are
+// strided in the host arrays (nh of H heads per token): 2-D copies move
+// them to and from compact staging buffers.  Per chunk, on kHostSets
+// staging sets in turn: q, k, v copied in on the copy-in stream (once the
+// set's previous chunk has been computed); `compute` queued on the caller's
+// stream or the second compute stream in turn (one chunk's last wave
+// overlaps the next chunk's first), once the inputs are in and the set's
+// previous outputs have left; o and lse copied out on the copy-out stream.
+// A set holds q, k, v, o, lse of up to one batch entry and `extra_bytes`
+// more for `compute`; `pre_bytes` from `pre_src` (host) go once to a
+// device area after the sets, before the first chunk.
+template <class Compute>
+attn_status_t host_pipeline(DeviceState *ds, const void *q, const void *k, const void *v, void *o,
+                            float *lse, int B, int H, int N, int d, size_t extra_bytes,
+                            const void *pre_src, size_t pre_bytes, cudaStream_t s,
+                            Compute compute) {
+  constexpr int S = DeviceState::kHostSets;
+  const size_t row = static_cast<size_t>(H) * d * 2;            // one token of q, k, v or o
+  const size_t per_b = static_cast<size_t>(N) * row;            // one batch entry
+  const size_t lse_b = static_cast<size_t>(H) * N * sizeof(float);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t set_bytes = 4 * up(per_b) + up(lse_b) + up(extra_bytes);
+  attn_status_t st = grow_workspace(&ds->host_ws, &ds->host_ws_bytes, S * set_bytes + up(pre_bytes));
+  if (st != ATTN_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (ds->h2d == nullptr) {
+      if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&ds->comp2, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ds->ev_start, cudaEventDisableTiming) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      for (int i = 0; i < S; ++i)
+        if (cudaEventCreateWithFlags(&ds->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ds->ev_comp[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ds->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+          return ATTN_ERR_CUDA;
+    }
+  }
+  const int nqt = (N + 255) / 256;
+  int hg = H;
+  for (int x = 1; x < H; ++x)
+    if (H % x == 0 && static_cast<long long>(x) * nqt >= ds->num_sms) {
+      hg = x;
+      break;
+    }
+  std::vector<HostChunk> chunks;
+  for (int b = 0; b < B; ++b) {
+    if ((b == 0 || b == B - 1) && hg < H)
+      for (int h0 = 0; h0 < H; h0 += hg) chunks.push_back({b, h0, hg});
+    else
+      chunks.push_back({b, 0, H});
+  }
+  const char *qh = static_cast<const char *>(q), *kh = static_cast<const char *>(k);
+  const char *vh = static_cast<const char *>(v);
+  char *oh = static_cast<char *>(o);
+  char *ws = reinterpret_cast<char *>(ds->host_ws);
+  char *pre = ws + S * set_bytes;
+  bool ok = true;
+  auto chk = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // everything queued on the caller's stream before this call comes first
+  chk(cudaEventRecord(ds->ev_start, s));
+  chk(cudaStreamWaitEvent(ds->h2d, ds->ev_start, 0));
+  if (pre_bytes > 0) chk(cudaMemcpyAsync(pre, pre_src, pre_bytes, cudaMemcpyHostToDevice, ds->h2d));
+  const int nc = static_cast<int>(chunks.size());
+  int last_set = 0;
+  for (int c = 0; ok && c < nc; ++c) {
+    const HostChunk ch = chunks[c];
+    const int set = c % S;
+    last_set = set;
+    char *dq = ws + set * set_bytes, *dk = dq + up(per_b), *dv = dk + up(per_b);
+    char *dout = dv + up(per_b);
+    float *dlse = reinterpret_cast<float *>(dout + up(per_b));
+    char *extra = dout + up(per_b) + up(lse_b);
+    const size_t w = static_cast<size_t>(ch.nh) * d * 2;        // bytes of a chunk row
+    const size_t hoff = static_cast<size_t>(ch.b) * per_b + static_cast<size_t>(ch.h0) * d * 2;
+    // inputs, once chunk c - S (same set) has been computed (one copy
+    // stream: a second one measured slower, the two share the host link)
+    if (c >= S) chk(cudaStreamWaitEvent(ds->h2d, ds->ev_comp[set], 0));
+    chk(cudaMemcpy2DAsync(dq, w, qh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpy2DAsync(dk, w, kh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaMemcpy2DAsync(dv, w, vh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
+    chk(cudaEventRecord(ds->ev_in[set], ds->h2d));
+    cudaStream_t cs = (c & 1) ? ds->comp2 : s;
+    chk(cudaStreamWaitEvent(cs, ds->ev_in[set], 0));
+    if (c >= S) chk(cudaStreamWaitEvent(cs, ds->ev_out[set], 0));
+    if (!ok) break;
+    if ((st = compute(ch, dq, dk, dv, dout, lse ? dlse : nullptr, extra, pre, cs)) != ATTN_OK)
+      return st;
+    chk(cudaEventRecord(ds->ev_comp[set], cs));
+    // outputs of the chunk
+    chk(cudaStreamWaitEvent(ds->d2h, ds->ev_comp[set], 0));
+    chk(cudaMemcpy2DAsync(oh + hoff, row, dout, w, w, N, cudaMemcpyDeviceToHost, ds->d2h));
+    if (lse)
+      chk(cudaMemcpyAsync(lse + (static_cast<size_t>(ch.b) * H + ch.h0) * N, dlse,
+                          static_cast<size_t>(ch.nh) * N * sizeof(float), cudaMemcpyDeviceToHost,
+                          ds->d2h));
+    chk(cudaEventRecord(ds->ev_out[set], ds->d2h));
+  }
+  // later work on the caller's stream sees the outputs (the copy-out stream
+  // runs in order and every copy-out follows its chunk's compute, so its
+  // last event covers both compute streams)
+  if (ok) chk(cudaStreamWaitEvent(s, ds->ev_out[last_set], 0));
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -307,106 +423,17 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
   if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d > (1LL << 40) / B) return ATTN_ERR_TOO_LARGE;
-  constexpr int S = DeviceState::kHostSets;
-  const size_t row = static_cast<size_t>(H) * d * 2;            // one token of q, k, v or o
-  const size_t per_b = static_cast<size_t>(N) * row;            // one batch entry
-  const size_t lse_b = static_cast<size_t>(H) * N * sizeof(float);
-  // one staging set: q, k, v, o and lse of up to one batch entry, 256-byte
-  // aligned parts
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t set_bytes = 4 * up(per_b) + up(lse_b);
   DeviceState *ds = nullptr;
   if ((st = device_state(&ds)) != ATTN_OK) return st;
-  if ((st = grow_workspace(&ds->host_ws, &ds->host_ws_bytes, S * set_bytes)) != ATTN_OK) return st;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (ds->h2d == nullptr) {
-      if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
-          cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
-          cudaStreamCreateWithFlags(&ds->comp2, cudaStreamNonBlocking) != cudaSuccess ||
-          cudaEventCreateWithFlags(&ds->ev_start, cudaEventDisableTiming) != cudaSuccess)
-        return ATTN_ERR_CUDA;
-      for (int i = 0; i < S; ++i)
-        if (cudaEventCreateWithFlags(&ds->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ds->ev_comp[i], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ds->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
-          return ATTN_ERR_CUDA;
-    }
-  }
-  // Work items ("chunks"): whole batch entries, except that the first and
-  // the last entry are cut into groups of hg heads -- the fewest heads whose
-  // 256-row tiles still fill every SM once -- so the compute starts after a
-  // smaller first copy and what is left after the last copy is short.  A
-  // chunk's rows are strided in the host arrays (hg of H heads per token):
-  // 2-D copies move them to and from compact staging buffers.
-  const int nqt = (N + 255) / 256;
-  int hg = H;
-  for (int x = 1; x < H; ++x)
-    if (H % x == 0 && static_cast<long long>(x) * nqt >= ds->num_sms) {
-      hg = x;
-      break;
-    }
-  struct Chunk { int b, h0, nh; };
-  std::vector<Chunk> chunks;
-  for (int b = 0; b < B; ++b) {
-    if ((b == 0 || b == B - 1) && hg < H)
-      for (int h0 = 0; h0 < H; h0 += hg) chunks.push_back({b, h0, hg});
-    else
-      chunks.push_back({b, 0, H});
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const char *qh = static_cast<const char *>(q), *kh = static_cast<const char *>(k);
-  const char *vh = static_cast<const char *>(v);
-  char *oh = static_cast<char *>(o);
-  char *ws = reinterpret_cast<char *>(ds->host_ws);
-  bool ok = true;
-  auto chk = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
-  // everything queued on the caller's stream before this call comes first
-  chk(cudaEventRecord(ds->ev_start, s));
-  chk(cudaStreamWaitEvent(ds->h2d, ds->ev_start, 0));
-  const int nc = static_cast<int>(chunks.size());
-  int last_set = 0;
-  for (int c = 0; ok && c < nc; ++c) {
-    const Chunk ch = chunks[c];
-    const int set = c % S;
-    last_set = set;
-    char *dq = ws + set * set_bytes, *dk = dq + up(per_b), *dv = dk + up(per_b);
-    char *dout = dv + up(per_b);
-    float *dlse = reinterpret_cast<float *>(dout + up(per_b));
-    const size_t w = static_cast<size_t>(ch.nh) * d * 2;        // bytes of a chunk row
-    const size_t hoff = static_cast<size_t>(ch.b) * per_b + static_cast<size_t>(ch.h0) * d * 2;
-    // inputs, once chunk c - S (same set) has been computed (one copy
-    // stream: a second one measured slower, the two share the host link)
-    if (c >= S) chk(cudaStreamWaitEvent(ds->h2d, ds->ev_comp[set], 0));
-    chk(cudaMemcpy2DAsync(dq, w, qh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
-    chk(cudaMemcpy2DAsync(dk, w, kh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
-    chk(cudaMemcpy2DAsync(dv, w, vh + hoff, row, w, N, cudaMemcpyHostToDevice, ds->h2d));
-    chk(cudaEventRecord(ds->ev_in[set], ds->h2d));
-    // compute on the caller's stream and the second compute stream in turn
-    // (one chunk's last wave overlaps the next chunk's first), once the
-    // inputs are in and chunk c - S's outputs have left the set
-    cudaStream_t cs = (c & 1) ? ds->comp2 : s;
-    chk(cudaStreamWaitEvent(cs, ds->ev_in[set], 0));
-    if (c >= S) chk(cudaStreamWaitEvent(cs, ds->ev_out[set], 0));
-    if (!ok) break;
-    if ((st = fwd_dense(dq, dk, dv, dout, lse ? dlse : nullptr, 1, ch.nh, ch.nh, N, d, scale,
-                        causal, dtype, false, cs)) != ATTN_OK)
-      return st;
-    chk(cudaEventRecord(ds->ev_comp[set], cs));
-    // outputs of the chunk
-    chk(cudaStreamWaitEvent(ds->d2h, ds->ev_comp[set], 0));
-    chk(cudaMemcpy2DAsync(oh + hoff, row, dout, w, w, N, cudaMemcpyDeviceToHost, ds->d2h));
-    if (lse)
-      chk(cudaMemcpyAsync(lse + (static_cast<size_t>(ch.b) * H + ch.h0) * N, dlse,
-                          static_cast<size_t>(ch.nh) * N * sizeof(float), cudaMemcpyDeviceToHost,
-                          ds->d2h));
-    chk(cudaEventRecord(ds->ev_out[set], ds->d2h));
-  }
-  // later work on the caller's stream sees the outputs (the copy-out stream
-  // runs in order and every copy-out follows its chunk's compute, so its
-  // last event covers both compute streams)
-  if (ok) chk(cudaStreamWaitEvent(s, ds->ev_out[last_set], 0));
-  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+  // each chunk: the dense forward on its compact buffers, the last wave
+  // whole (two chunks may run at once; the split workspace is shared)
+  auto compute = [&](const HostChunk &ch, char *dq, char *dk, char *dv, char *dout, float *dlse,
+                     char *, char *, cudaStream_t cs) {
+    return fwd_dense(dq, dk, dv, dout, dlse, 1, ch.nh, ch.nh, N, d, scale, causal, dtype, false,
+                     cs);
+  };
+  return host_pipeline(ds, q, k, v, o, lse, B, H, N, d, 0, nullptr, 0,
+                       static_cast<cudaStream_t>(stream), compute);
 }
 
 attn_status_t attn_fwd_varlen_gqa(const void *q, const void *k, const void *v, void *o,
@@ -449,9 +476,11 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
                              d, scale, causal, dtype, stream);
 }
 
-attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *descale_q,
-                           const float *descale_k, const float *descale_v, void *o, float *lse,
-                           int B, int H, int N, int d, float scale, int causal, void *stream) {
+// The e4m3 forward; allow_split as for fwd_dense.
+static attn_status_t fwd_fp8(const void *q8, const void *k8, const void *v8,
+                             const float *descale_q, const float *descale_k,
+                             const float *descale_v, void *o, float *lse, int B, int H, int N,
+                             int d, float scale, int causal, bool allow_split, cudaStream_t s) {
   attn_status_t st = check_common(q8, k8, v8, o, lse, H, d, scale);
   if (st != ATTN_OK) return st;
   if (B < 1 || N < 1 || !descale_q || !descale_k || !descale_v) return ATTN_ERR_INVALID_ARG;
@@ -469,8 +498,49 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const
   a.num_tiles = static_cast<int>(tiles);
   a.dq = descale_q; a.dk = descale_k; a.dv = descale_v;
   a.status = ds->status; a.budget = wait_budget(); a.num_sms = ds->num_sms;
-  if ((st = plan_tail_split(ds, a)) != ATTN_OK) return st;
-  return launch_attn_e4m3(a, static_cast<cudaStream_t>(stream));
+  if (allow_split && (st = plan_tail_split(ds, a)) != ATTN_OK) return st;
+  return launch_attn_e4m3(a, s);
+}
+
+attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *descale_q,
+                           const float *descale_k, const float *descale_v, void *o, float *lse,
+                           int B, int H, int N, int d, float scale, int causal, void *stream) {
+  return fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
+                 true, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_fp8_host(const void *q, const void *k, const void *v, const int8_t *signs,
+                                void *o, float *lse, int B, int H, int N, int d, float scale,
+                                int causal, void *stream) {
+  attn_status_t st = check_common(q, k, v, o, lse, H, d, scale);
+  if (st != ATTN_OK) return st;
+  if (B < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(N) * H * d > (1LL << 40) / B) return ATTN_ERR_TOO_LARGE;
+  DeviceState *ds = nullptr;
+  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const int nblk = (N + 127) / 128;
+  const size_t code_b = up(static_cast<size_t>(N) * H * d);             // e4m3 codes of one entry
+  const size_t dsc_b = up(static_cast<size_t>(H) * nblk * sizeof(float));
+  // each chunk: block quantisation (with the rotation when signs are given)
+  // of its compact q, k, v, then the e4m3 forward, the last wave whole
+  auto compute = [&](const HostChunk &ch, char *dq, char *dk, char *dv, char *dout, float *dlse,
+                     char *extra, char *pre, cudaStream_t cs) {
+    char *q8 = extra, *k8 = q8 + code_b, *v8 = k8 + code_b;
+    float *dsq = reinterpret_cast<float *>(v8 + code_b);
+    float *dsk = reinterpret_cast<float *>(reinterpret_cast<char *>(dsq) + dsc_b);
+    float *dsv = reinterpret_cast<float *>(reinterpret_cast<char *>(dsk) + dsc_b);
+    attn_status_t r = qkv_block_quant_hadamard(dq, dk, dv, q8, k8, v8, dsq, dsk, dsv,
+                                               signs ? reinterpret_cast<const int8_t *>(pre)
+                                                     : nullptr,
+                                               0, 1, ch.nh, N, d, cs);
+    if (r != ATTN_OK) return r;
+    return fwd_fp8(q8, k8, v8, dsq, dsk, dsv, dout, dlse, 1, ch.nh, N, d, scale, causal, false,
+                   cs);
+  };
+  return host_pipeline(ds, q, k, v, o, lse, B, H, N, d, 3 * code_b + 3 * dsc_b, signs,
+                       signs ? static_cast<size_t>(d) : 0, static_cast<cudaStream_t>(stream),
+                       compute);
 }
 
 attn_status_t attn_get_status(void *stream) {

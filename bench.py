@@ -256,9 +256,17 @@ def build_step(w, dev):
     if (not w.varlen and w.dtype in ("bf16", "fp16") and w.Hkv in (None, w.H)
             and not w.name.startswith("bf16 backward")):
         # dense 16-bit: the host-buffer entry point, which overlaps the copies
-        # of one batch entry with the compute of the previous one
+        # of each chunk (batch entries, head groups at both ends) with the
+        # compute of earlier chunks
         def e2e():
             agb.attn_fwd_host(hq, hk, hv, causal=w.causal, out=ho, lse=hl)
+    elif w.dtype == "fp8" and not w.varlen:
+        # the 8-bit path's host-buffer entry point: per chunk, bf16 in,
+        # quantisation and the e4m3 forward on the device, bf16 out
+        hsigns = torch.from_numpy(x["signs"])
+
+        def e2e():
+            agb.attn_fwd_fp8_host(hq, hk, hv, signs=hsigns, causal=w.causal, out=ho, lse=hl)
     else:
         def e2e():
             q.copy_(hq, non_blocking=True)

@@ -282,6 +282,26 @@ attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void 
                                        int B, int H, int N, int d, void *stream);
 
 /*
+ * The 8-bit path on HOST buffers: qkv_block_quant_hadamard (block scales,
+ * per_tensor = 0) and attn_fwd_fp8 for data that lives in host memory.
+ *   q, k, v : HOST [B, N, H, d] bf16;  o : HOST [B, N, H, d] bf16;
+ *   lse     : HOST [B, H, N] float32 (may be NULL).
+ *   signs   : HOST int8 [d] of +1/-1 (the random sign diagonal), or NULL for
+ *             no rotation; copied to the device by the call.
+ * The work moves in the chunks of attn_fwd_host (batch entries, and head
+ * groups of the first and last entry): each chunk is copied in, quantised
+ * with one scale per 128-token block of each (b, h) -- so the codes and
+ * scales equal those of the whole tensor -- computed by the e4m3 kernel
+ * with its last wave whole, and copied out, overlapped with the other
+ * chunks' copies and compute.  Staging (bf16 inputs, codes, scales,
+ * outputs) lives in the per-device workspace.  Stream order, page-locked
+ * memory and errors as attn_fwd_host; d = 64 or 128.
+ */
+attn_status_t attn_fwd_fp8_host(const void *q, const void *k, const void *v,
+                                const int8_t *signs, void *o, float *lse, int B, int H, int N,
+                                int d, float scale, int causal, void *stream);
+
+/*
  * Backward pass: gradients of the dense forward (attn_fwd / attn_fwd_gqa)
  * with respect to Q, K and V, given the upstream gradient dO (the backward
  * pass of the FlashAttention-3 summary, arxivlens, Key Results; "backward

@@ -81,6 +81,12 @@ def test_varlen_fp8_quant_reject_bad_arguments(L):
     assert hst(FAKE, FAKE, FAKE, FAKE, None, 0, 4, 16, 64, 0.1, 0, 0, None) == 1
     assert hst(FAKE, FAKE, FAKE, FAKE, None, 2, 4, 16, 96, 0.1, 0, 0, None) == 2
     assert hst(FAKE, FAKE, FAKE + 4, FAKE, None, 2, 4, 16, 64, 0.1, 0, 0, None) == 3
+    fh = L.attn_fwd_fp8_host
+    #        q     k     v     signs o     lse   B  H  N   d    scale causal stream
+    assert fh(None, FAKE, FAKE, None, FAKE, None, 2, 4, 16, 128, 0.1, 0, None) == 1
+    assert fh(FAKE, FAKE, FAKE, None, FAKE, None, 2, 4, 0, 128, 0.1, 0, None) == 1
+    assert fh(FAKE, FAKE, FAKE, None, FAKE, None, 2, 4, 16, 96, 0.1, 0, None) == 2
+    assert fh(FAKE, FAKE, FAKE, None, FAKE + 4, None, 2, 4, 16, 128, 0.1, 0, None) == 3
     f = L.attn_fwd_fp8
     assert f(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 1, 1, 16, 128, 0.1, 0, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 16, 96, 0.1, 0, None) == 2

@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import attention_forward_softmax_gb300 as agb
+from datagen import random_signs
 from tests._gpu_helpers import qkv
 
 pytestmark = pytest.mark.gpu
@@ -97,3 +98,40 @@ def test_host_path_outputs_are_ordered_on_the_stream():
     o_ref, _ = device_reference(q, k, v, False)
     assert torch.equal(o_dev.cpu().view(torch.int16), o_ref.view(torch.int16))
     assert np.isfinite(lse.numpy()).all()
+
+
+def fp8_device_reference(q, k, v, signs, causal):
+    q8, k8, v8, dq, dk, dv = agb.qkv_block_quant_hadamard(
+        q.cuda(), k.cuda(), v.cuda(), None if signs is None else signs.cuda())
+    o, lse = agb.attn_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=causal)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+def fp8_no_split(B, H, N, d):
+    """attn_fwd_fp8 leaves every tile whole at this shape (non-causal)."""
+    return d != 128 or no_split(B, H, N)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,rot", [
+    (2, 32, 4096, 128, False, True),      # head groups at both ends
+    (3, 48, 4096, 128, True, True),
+    (3, 4, 700, 128, False, False),       # whole entries, ragged blocks, no rotation
+    (2, 3, 300, 64, True, True),
+])
+def test_fp8_host_path_matches_device_path_bitwise(B, H, N, d, causal, rot):
+    """attn_fwd_fp8_host quantises each chunk (block scales per (b, h,
+    128-token block): the same codes and scales as the whole tensor) and runs
+    the e4m3 kernel on it; at shapes where attn_fwd_fp8 splits nothing the
+    outputs are bitwise those of the device path."""
+    if not causal and not fp8_no_split(B, H, N, d):
+        pytest.skip("attn_fwd_fp8 would split the last wave at this SM count")
+    q, k, v = qkv(9540 + H + d, (B, N, H, d), torch.bfloat16)
+    signs = torch.from_numpy(random_signs(9541, d)) if rot else None
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o, lse = agb.attn_fwd_fp8_host(hq, hk, hv, signs=signs, causal=causal)
+    torch.cuda.current_stream().synchronize()
+    assert agb.get_status() == 0
+    o_ref, lse_ref = fp8_device_reference(q, k, v, signs, causal)
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
