@@ -632,7 +632,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ++s_cnt;
         tc_fence_after();
         uint32_t sv[128];
-        tmem_ld128(tS, sv);
+        float mx_ld;                      // row maximum, from the load itself
+        tmem_ld128_max(tS, sv, mx_ld);
         // S is in registers: the tensor core may overwrite it
         tc_fence_before();
         mbar_arrive(&bar_s_free[x]);
@@ -657,18 +658,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
-        }
-        // row maximum: four independent three-input chains
-        float mx4[4];
+          // row maximum of the masked row: four independent three-input chains
+          float mx4[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t *sc = sv + 32 * c;
-          float m = fmaxf(__uint_as_float(sc[0]), __uint_as_float(sc[1]));
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t *sc = sv + 32 * c;
+            float m = fmaxf(__uint_as_float(sc[0]), __uint_as_float(sc[1]));
 #pragma unroll
-          for (int i = 2; i < 32; i += 2) m = fmax3(m, __uint_as_float(sc[i]), __uint_as_float(sc[i + 1]));
-          mx4[c] = m;
+            for (int i = 2; i < 32; i += 2) m = fmax3(m, __uint_as_float(sc[i]), __uint_as_float(sc[i + 1]));
+            mx4[c] = m;
+          }
+          mx_ld = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         }
-        const float m_tile = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
+        const float m_tile = mx_ld * cs;
         const float m_new = fmaxf(m_run, m_tile);
         const bool resc = m_new > m_run + C::kRescaleThresh;
         float alpha = 1.f;
@@ -801,7 +803,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ++s_cnt;
         tc_fence_after();
         uint32_t sv[128];
-        tmem_ld128(tS, sv);              // the whole score row in one round trip
+        float mx;                        // row maximum, from the load itself
+        tmem_ld128_max(tS, sv, mx);      // the whole score row in one round trip
         if constexpr (C::kSepP) {        // S is in registers: the tensor core may overwrite it
           tc_fence_before();
           mbar_arrive(&bar_s_free[x]);
@@ -846,18 +849,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (kbase + i >= lim) sv[i] = __float_as_uint(-INFINITY);
         }
-        // row max: four independent chains of three-input maxima
-        float mq[4];
+        if (C::kBias || need_mask) {
+          // the row changed after the load: its maximum from four independent
+          // chains of three-input maxima
+          float mq[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mq[u] = __uint_as_float(sv[32 * u]);
+          for (int u = 0; u < 4; ++u) mq[u] = __uint_as_float(sv[32 * u]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 1; i < 31; i += 2)
-            mq[c] = fmax3(mq[c], __uint_as_float(sv[32 * c + i]), __uint_as_float(sv[32 * c + i + 1]));
+            for (int i = 1; i < 31; i += 2)
+              mq[c] = fmax3(mq[c], __uint_as_float(sv[32 * c + i]), __uint_as_float(sv[32 * c + i + 1]));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mq[c] = fmaxf(mq[c], __uint_as_float(sv[32 * c + 31]));
-        const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+          for (int c = 0; c < 4; ++c) mq[c] = fmaxf(mq[c], __uint_as_float(sv[32 * c + 31]));
+          mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+        }
         const float m_tile = mx * cs;
         const float m_new = fmaxf(m_run, m_tile);
         const bool resc = m_new > m_run + C::kRescaleThresh;
