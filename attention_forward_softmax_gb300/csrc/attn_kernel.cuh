@@ -106,8 +106,8 @@ struct Cfg {
   static constexpr int kSmemBudget = 224 * 1024;
   // K/V ring: the largest power of two of tiles (at most 8) that fits beside
   // the two Q sub-tiles and, for e4m3, the two P tiles
-  static constexpr int kRingFit = (kSmemBudget - 2 * kTileBytes - 2 * (kFp8 ? 128 * 128 : 0)) /
-                                  kTileBytes;
+  static constexpr int kRingFit =
+      (kSmemBudget - 2 * kTileBytes - 2 * (kFp8 ? 2 * 128 * 128 : 0)) / kTileBytes;
   static constexpr int NS = kRingFit >= 8 ? 8 : (kRingFit >= 4 ? 4 : 2);
   static_assert(NS >= 3, "K/V ring too small");
   static_assert((NS & (NS - 1)) == 0, "K/V ring size must be a power of two");
@@ -141,6 +141,9 @@ struct Cfg {
   // softmax has read it; 16-bit P stays in TMEM over S.
   static constexpr bool kSmemP = kFp8;
   static constexpr int kPTileBytes = kSmemP ? 128 * 128 : 0;
+  // P tiles per sub-tile: two for e4m3, so the exponentials of a block do
+  // not wait for the O update that reads the previous block's P
+  static constexpr int kPBufs = kSmemP ? 2 : 1;
   // 16-bit at d = 64: O_A and O_B take only 128 TMEM columns, so P gets its
   // own 64 columns per sub-tile after them and S is free once it is read,
   // as in the e4m3 path (P in TMEM rather than shared memory).
@@ -160,8 +163,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffP = kOffKV + NS * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPTileBytes;
-  static constexpr int kNumBars = 2 + 2 * NS + 13;
+  static constexpr int kOffBar = kOffP + 2 * kPBufs * kPTileBytes;
+  static constexpr int kNumBars = 2 + 2 * NS + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024 /* alignment slack */ + 1024 /* guard */;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeded");
@@ -289,6 +292,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t *bar_drain = bar_s_full + 8;
   uint64_t *bar_s_free = bar_s_full + 9;           // [2] e4m3: softmax has read S
   uint64_t *bar_o_done = bar_s_full + 11;          // [2] e4m3, d = 64: an O update completed
+  // e4m3, second P tile of each sub-tile: its P-full and O-done barriers
+  uint64_t *bar_p_full1 = bar_s_full + 13;         // [2]
+  uint64_t *bar_o_done1 = bar_s_full + 15;         // [2]
+  // the barriers of P tile b of sub-tile x
+  auto p_full_bar = [&](int x, int b) { return b ? &bar_p_full1[x] : &bar_p_full[x]; };
+  auto o_done_bar = [&](int x, int b) { return b ? &bar_o_done1[x] : &bar_o_done[x]; };
   uint8_t *sP = smem + C::kOffP;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -314,6 +323,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_free[x], C::kSoftArrive);
       mbar_init(&bar_o_done[x], 1);
+      mbar_init(&bar_p_full1[x], C::kSoftArrive);
+      mbar_init(&bar_o_done1[x], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -445,9 +456,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // O_X (+)= P_X V with P_X in shared memory (e4m3 path)
       const uint64_t p0d = sdesc_sw128(smem_addr(sP), 16, 1024);
       const uint32_t p_lo = static_cast<uint32_t>(p0d), p_hi = static_cast<uint32_t>(p0d >> 32);
-      auto issue_pv_smem = [&](int x, unsigned pos, bool accumulate) {
+      auto issue_pv_smem = [&](int x, int pb, unsigned pos, bool accumulate) {
         const uint32_t va = v_lo + (pos & (C::NS - 1)) * (C::kTileBytes >> 4);
-        const uint32_t pa = p_lo + static_cast<uint32_t>(x * (C::kPTileBytes >> 4));
+        const uint32_t pa =
+            p_lo + static_cast<uint32_t>((x * C::kPBufs + pb) * (C::kPTileBytes >> 4));
         const uint32_t d = tmem + C::kColO0 + x * C::D;
         mma_f8_ss(d, desc(pa, p_hi), desc(va, v_hi), C::kIdescPV, accumulate);
 #pragma unroll
@@ -468,8 +480,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after();
         return true;
       };
+      // P tile c of sub-tile x (counted over the whole run) is buffer
+      // c mod kPBufs, whose barrier completes for it for the (c / kPBufs)-th
+      // time
       auto wait_p = [&](int x) {
-        if (!mbar_wait(&bar_p_full[x], p_cnt[x] & 1, wc)) return false;
+        const unsigned c = p_cnt[x];
+        if (!mbar_wait(p_full_bar(x, c % C::kPBufs), (c / C::kPBufs) & 1, wc)) return false;
         ++p_cnt[x];
         tc_fence_after();
         return true;
@@ -509,10 +525,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const unsigned pv = kv_pos + 2 * j + 1;
             if (!wait_kv(pv)) { ok = false; break; }
             if (j == 0 && !mbar_wait(&bar_o_free[x], (tcount & 1) ^ 1, wc)) { ok = false; break; }
+            const int pb = static_cast<int>(p_cnt[x] % C::kPBufs);
             if (!wait_p(x)) { ok = false; break; }
-            if constexpr (C::kSmemP) issue_pv_smem(x, pv, j > 0);
+            if constexpr (C::kSmemP) issue_pv_smem(x, pb, pv, j > 0);
             else issue_pv(x, pv, j > 0);
-            mma_commit(&bar_o_done[x]);
+            mma_commit(o_done_bar(x, pb));
             if (j == nX - 1) mma_commit(&bar_o_final[x]);
             mma_commit(&bar_kv_empty[pv & (C::NS - 1)]);
           }
@@ -599,7 +616,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + x * C::kColS;
     const uint32_t tO = tmem + lane_base + C::kColO0 + x * C::D;
-    const uint32_t p_row = smem_addr(sP) + x * C::kPTileBytes + r_in * 128;
+    const uint32_t p_row0 = smem_addr(sP) + x * C::kPBufs * C::kPTileBytes + r_in * 128;
     int s_cnt = 0, tcount = 0;
     unsigned pstore_cnt = 0;
     bool ok = true;
@@ -679,15 +696,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           l_run *= alpha;
           m_run = m_new;
         }
-        // The previous O_X update must be complete before O_X is rescaled
-        // and before its P tile is overwritten.
-        if (pstore_cnt > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&bar_o_done[x], (pstore_cnt - 1) & 1, wc))) {
+        // P tile pc (of this sub-tile, counted over the run) goes to buffer
+        // pb = pc mod 2, once the O update that read tile pc - 2 from it is
+        // complete
+        const unsigned pc = pstore_cnt++;
+        const int pb = static_cast<int>(pc & 1);
+        if (pc >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait(o_done_bar(x, pb), ((pc >> 1) - 1) & 1, wc))) {
           ok = false;
           break;
         }
-        ++pstore_cnt;
         tc_fence_after();
+        const uint32_t p_row = p_row0 + pb * C::kPTileBytes;
         // stored value p * pw = 2^(s*cs - m + log2 pw), the prescale folded
         // into the exponent; row sums of the stored values in packed fp32,
         // divided by pw once per key block
@@ -713,9 +733,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           st_shared_v4(p_row + ((c ^ (r_in & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_smem();
-        // Rescale O_X (the previous update has landed, and O_X += P_X(j) V_j
-        // waits for the arrival below).
+        // Rescale O_X once it holds every earlier update (the update of
+        // tile pc - 1 completes after all before it: one issuing thread,
+        // MMAs in order); O_X += P_X(j) V_j waits for the arrival below.
         if (j > 0 && (unit_f != 1.f || __any_sync(0xffffffffu, resc))) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(o_done_bar(x, static_cast<int>((pc - 1) & 1)),
+                                    ((pc - 1) >> 1) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float f = alpha * unit_f;
 #pragma unroll 1
           for (int c = 0; c < C::D / 32; ++c) {
@@ -727,7 +755,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bar_p_full[x]);
+        mbar_arrive(p_full_bar(x, pb));
         // the row sum is not needed by the O update: after the arrival
         l_run += (((ra[0] + rb[0]) + (ra[1] + rb[1])) + ((ra[2] + rb[2]) + (ra[3] + rb[3]))) *
                  ex2(-lpw);
