@@ -263,7 +263,7 @@ def build_step(w, dev):
     elif w.dtype == "fp8" and not w.varlen:
         # the 8-bit path's host-buffer entry point: per chunk, bf16 in,
         # quantisation and the e4m3 forward on the device, bf16 out
-        hsigns = torch.from_numpy(x["signs"])
+        hsigns = torch.from_numpy(x["signs"]).pin_memory()
 
         def e2e():
             agb.attn_fwd_fp8_host(hq, hk, hv, signs=hsigns, causal=w.causal, out=ho, lse=hl)

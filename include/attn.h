@@ -287,7 +287,9 @@ attn_status_t qkv_block_quant_hadamard(const void *q, const void *k, const void 
  *   q, k, v : HOST [B, N, H, d] bf16;  o : HOST [B, N, H, d] bf16;
  *   lse     : HOST [B, H, N] float32 (may be NULL).
  *   signs   : HOST int8 [d] of +1/-1 (the random sign diagonal), or NULL for
- *             no rotation; copied to the device by the call.
+ *             no rotation; copied to the device by the call (page-locked, like
+ *             the other host buffers, so that the call does not wait for
+ *             earlier work on the copy stream).
  * The work moves in the chunks of attn_fwd_host (batch entries, and head
  * groups of the first and last entry): each chunk is copied in, quantised
  * with one scale per 128-token block of each (b, h) -- so the codes and
