@@ -55,7 +55,8 @@ def no_split(B, H, N):
     return rem == 0 or 2 * rem > grid
 
 
-@pytest.mark.parametrize("B,H,N,causal", [(2, 32, 4096, False), (3, 48, 4096, True)])
+@pytest.mark.parametrize("B,H,N,causal", [(2, 32, 4096, False), (3, 48, 4096, True),
+                                             (1, 32, 4096, True)])
 def test_host_path_head_group_chunks(B, H, N, causal):
     """Shapes whose 256-row tiles fill the SMs with fewer heads than H, so
     the first and last entries move as head groups (strided 2-D copies)."""
@@ -118,6 +119,7 @@ def fp8_no_split(B, H, N, d):
     (3, 48, 4096, 128, True, True),
     (3, 4, 700, 128, False, False),       # whole entries, ragged blocks, no rotation
     (2, 3, 300, 64, True, True),
+    (1, 32, 4096, 128, True, True),       # one entry, cut into head groups
 ])
 def test_fp8_host_path_matches_device_path_bitwise(B, H, N, d, causal, rot):
     """attn_fwd_fp8_host quantises each chunk (block scales per (b, h,
