@@ -15,8 +15,11 @@ value = attention FLOPs (4 B H N^2 d, halved when causal) of all ranks / max
 over ranks of the device time of K steps (CUDA events on the launching stream,
 barrier + synchronize on both sides).  `e2e` repeats the measurement through
 the public API with the inputs copied from pinned host memory and O, lse
-copied back inside the timed region.  `--impl reference` times the fp64 CPU
-oracle on a bounded sample of the same workload instead.
+copied back inside the timed region: the host-buffer entry points for the
+dense 16-bit workloads (attn_fwd_host) and the fp8 workload
+(attn_fwd_fp8_host), which overlap the copies with the compute, and copies
+around the device step for the others.  `--impl reference` times the fp64
+CPU oracle on a bounded sample of the same workload instead.
 
 The default line also carries an `fp8` block: the e4m3 workload (B=4 H=16
 N=8192 d=128) with its attention kernel against the fp8 dense peak and its
